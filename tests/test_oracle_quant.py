@@ -1,0 +1,268 @@
+"""Pins of the oracle's quantizers, dequantizer and MX scale layout.
+
+What fixes the expected values (not the oracle's own code):
+  * closed forms of the scale rule s = amax/V_max, 1/s in fp32: the amax
+    element of every group lands on +-V_max (code 0x7E/0xFE for E4M3,
+    0x7B/0xFB for E5M2) -- fp32 rounding moves amax*(1/s) by at most 3 ulp
+    around V_max, and V_max's neighbours are far;
+  * groups built with a known power-of-two amax, so the expected scale, the
+    expected MX exponent and the position of the max code are known in
+    advance for each group (this pins the scale layouts);
+  * s = 1 (static scaling) reduces the quantizer to the plain cast, compared
+    with torch's float8 cast;
+  * the error bound of round-to-nearest (unit roundoff printed on "FP8
+    Mixed-Precision Serving in Production") for quantize -> dequantize;
+  * the E4M3 underflow probe of the "FP8 Serving" guide, section 2;
+  * the MX tiled layout: a bijection with the positions of the documented
+    128x4 tile.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import BLOCK_128x128, E4M3, E5M2, MX32, SF_LINEAR, SF_TILED, TENSOR, TILE_1x128, TOKEN
+from fp8_block_scaled_04_gb300 import synth
+
+MAXC = {E4M3: 0x7E, E5M2: 0x7B}
+VMAX = {E4M3: 448.0, E5M2: 57344.0}
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def _f32(b):
+    return oracle.bf16_to_f32(b)
+
+
+def _groups(rows, cols, gran):
+    """Yield (row slice, col slice, scale index) for each group of a gran (not MX)."""
+    if gran == TENSOR:
+        yield slice(0, rows), slice(0, cols), 0
+    elif gran == TOKEN:
+        for r in range(rows):
+            yield slice(r, r + 1), slice(0, cols), r
+    elif gran == TILE_1x128:
+        for kb in range(cols // 128):
+            for r in range(rows):
+                yield slice(r, r + 1), slice(kb * 128, kb * 128 + 128), kb * rows + r
+    elif gran == BLOCK_128x128:
+        nkb = cols // 128
+        for rb in range((rows + 127) // 128):
+            for kb in range(nkb):
+                yield slice(rb * 128, min(rows, rb * 128 + 128)), slice(kb * 128, kb * 128 + 128), rb * nkb + kb
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("gran", [TENSOR, TOKEN, TILE_1x128, BLOCK_128x128])
+def test_amax_element_hits_vmax(fmt, gran):
+    x = synth.bf16_matrix(200, 384, 1.0, 11, 12, 0.02, 40.0)
+    q, s = oracle.quantize(x, fmt, gran)
+    xf = np.abs(_f32(x))
+    for rs, cs, si in _groups(200, 384, gran):
+        g = xf[rs, cs]
+        amax = g.max()
+        hit = q[rs, cs][g == amax] & 0x7F
+        assert np.all(hit == MAXC[fmt])
+        assert np.float32(amax) / np.float32(VMAX[fmt]) == s[si]
+        # no element of the group exceeds V_max after scaling, none saturates but the max
+        assert np.all((q[rs, cs][g < amax] & 0x7F) <= MAXC[fmt])
+
+
+@pytest.mark.parametrize("gran", [TOKEN, TILE_1x128, BLOCK_128x128])
+def test_scale_layout_with_known_group_amax(gran):
+    rows, cols = 256, 512
+    rng = np.random.default_rng(9)
+    x = rng.uniform(-0.5, 0.5, (rows, cols)).astype(np.float32)
+    expect = {}
+    for rs, cs, si in _groups(rows, cols, gran):
+        e = (si * 7) % 23 - 11  # distinct-ish power-of-two amax per group
+        g = x[rs, cs] * 2.0 ** e
+        r_rel = si % (rs.stop - rs.start)
+        c_rel = (si * 13) % (cs.stop - cs.start)
+        g[r_rel, c_rel] = 2.0 ** e  # the amax element, exactly 2^e
+        x[rs, cs] = g
+        expect[si] = (e, rs.start + r_rel, cs.start + c_rel)
+    xb = _bf16(x)
+    q, s = oracle.quantize(xb, E4M3, gran)
+    for si, (e, r, c) in expect.items():
+        # 2^e / 448 in fp32: 448 = 7 * 2^6, so the scale is 2^(e-6)/7 rounded once
+        assert s[si] == np.float32(2.0 ** (e - 6) / 7.0)
+        assert q[r, c] == 0x7E
+
+
+def test_mx_exponent_and_layout_with_known_group_amax():
+    rows, cols = 160, 384  # ragged in rows (160 = 128 + 32) and in 128-col blocks
+    ng = cols // 32
+    rng = np.random.default_rng(10)
+    x = rng.uniform(-0.25, 0.25, (rows, cols)).astype(np.float32)
+    js = {}
+    for r in range(rows):
+        for j in range(ng):
+            e = (r * 3 + j * 5) % 30 - 15
+            x[r, j * 32:(j + 1) * 32] *= 2.0 ** e
+            x[r, j * 32 + (r + j) % 32] = 2.0 ** e
+            js[(r, j)] = e
+    xb = _bf16(x)
+    ql, sl = oracle.quantize(xb, E4M3, MX32, SF_LINEAR)
+    qt, st = oracle.quantize(xb, E4M3, MX32, SF_TILED)
+    assert np.array_equal(ql, qt)
+    assert st.size == ((rows + 127) // 128) * ((ng + 3) // 4) * 512
+    for (r, j), e in js.items():
+        # 2^e / 448 = 2^(e-8) / 1.75 -> ceil(log2) = e - 8; SF byte = 127 + e - 8
+        b = 127 + e - 8
+        assert sl[r * ng + j] == b
+        assert st[((r // 128) * ((ng + 3) // 4) + j // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4] == b
+        # the amax element becomes 2^e * 2^-(e-8) = 256 = code 0x78 (E=15, M=0)
+        assert ql[r, j * 32 + (r + j) % 32] == 0x78
+
+
+def test_mx_amax_lands_in_upper_half_of_range():
+    x = synth.bf16_matrix(64, 1024, 1.0, 21, 22, 0.01, 80.0)
+    for fmt in (E4M3, E5M2):
+        q, sf = oracle.quantize(x, fmt, MX32)
+        xf = np.abs(_f32(x)).reshape(64, 32, 32)
+        dec = np.abs(oracle.decode(q, fmt)).reshape(64, 32, 32)
+        amax_idx = xf.argmax(axis=2)
+        top = np.take_along_axis(dec, amax_idx[..., None], axis=2)[..., 0]
+        # before rounding amax * 2^-e lies in (V/2, V]; rounding to the format keeps it in [V/2, V]
+        assert np.all(top >= VMAX[fmt] / 2) and np.all(top <= VMAX[fmt])
+        assert np.any(top > VMAX[fmt] / 2)
+
+
+def test_mx_exponent_closed_form():
+    for j in range(-20, 21):
+        assert oracle.mx_exponent(2.0 ** j, E4M3) == j - 8
+        assert oracle.mx_exponent(448.0 * 2.0 ** j, E4M3) == j  # exact power-of-two ratio: no ceil step
+        assert oracle.mx_exponent(448.0 * 2.0 ** j * 1.0000001, E4M3) == j + 1
+    assert oracle.mx_exponent(0.0, E4M3) == -127
+    assert oracle.mx_exponent(3.0e38, E4M3) == 120  # 3e38/448 ~ 2^119.3: ceil -> 120, no clamp needed
+    assert oracle.mx_exponent(3.0e38, E5M2) == 113
+    # bf16's smallest subnormal: ceil(log2(2^-133 / 448)) = -141 lies below UE8M0's range and clamps to -127
+    assert oracle.mx_exponent(2.0 ** -133, E4M3) == -127
+    assert oracle.mx_exponent(2.0 ** -110, E4M3) == -118  # fp32-normal ratio 2^-118.8 -> -118
+
+
+def test_mx_tiled_layout_is_documented_bijection():
+    rows, ng = 300, 13
+    nrb, ncb = (rows + 127) // 128, (ng + 3) // 4
+    size = oracle.mx_tiled_bytes(rows, ng)
+    assert size == nrb * ncb * 512
+    seen = np.zeros(size, dtype=np.int64)
+    for r in range(nrb * 128):
+        for j in range(ncb * 4):
+            seen[oracle.mx_tiled_offset(r, j, rows, ng)] += 1
+    assert np.all(seen == 1)
+    # positions inside one 128x4 tile: 32 lines of 16 bytes, line = row % 32,
+    # 4-byte word = (row / 32) % 4, byte = group % 4
+    assert oracle.mx_tiled_offset(0, 0, rows, ng) == 0
+    assert oracle.mx_tiled_offset(0, 3, rows, ng) == 3
+    assert oracle.mx_tiled_offset(1, 0, rows, ng) == 16
+    assert oracle.mx_tiled_offset(31, 0, rows, ng) == 496
+    assert oracle.mx_tiled_offset(32, 0, rows, ng) == 4
+    assert oracle.mx_tiled_offset(127, 3, rows, ng) == 31 * 16 + 3 * 4 + 3
+    assert oracle.mx_tiled_offset(0, 4, rows, ng) == 512
+    assert oracle.mx_tiled_offset(128, 0, rows, ng) == ncb * 512
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_static_unit_scale_is_plain_cast(fmt):
+    x = synth.bf16_matrix(64, 256, 3.0, 31)
+    q, s = oracle.quantize(x, fmt, TENSOR, static_scale=1.0)
+    assert s[0] == 1.0
+    ref = torch.from_numpy(_f32(x).copy()).to({E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}[fmt])
+    assert np.array_equal(q, ref.view(torch.uint8).numpy())
+
+
+def test_tensor_static_scale_used_verbatim():
+    x = synth.bf16_matrix(32, 128, 1.0, 41)
+    q, s = oracle.quantize(x, E4M3, TENSOR, static_scale=0.5)
+    assert s[0] == 0.5
+    ref = oracle.encode(_f32(x) * np.float32(2.0), E4M3)
+    assert np.array_equal(q, ref)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("gran", [TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32])
+def test_roundtrip_error_within_unit_roundoff(fmt, gran):
+    x = synth.bf16_matrix(130, 640, 1.0, 51, 52, 0.01, 60.0)
+    q, s = oracle.quantize(x, fmt, gran)
+    xh = _f32(oracle.dequantize(q, s, fmt, gran)).astype(np.float64)
+    xf = _f32(x).astype(np.float64)
+    u = 2.0 ** -4 if fmt == E4M3 else 2.0 ** -3
+    # per-element scale from the group max: values below the format's smallest
+    # normal (after scaling) are held to the subnormal spacing instead
+    if gran == MX32:
+        sc = np.repeat(2.0 ** (s.reshape(130, -1).astype(np.float64) - 127), 32, axis=1)
+    elif gran == TENSOR:
+        sc = np.full(xf.shape, float(s[0]))
+    elif gran == TOKEN:
+        sc = np.repeat(s.astype(np.float64)[:, None], 640, axis=1)
+    elif gran == TILE_1x128:
+        sc = np.repeat(s.reshape(5, 130).T.astype(np.float64), 128, axis=1)
+    else:
+        blk = s.reshape(2, 5).astype(np.float64)
+        sc = np.repeat(np.repeat(blk, 128, axis=0)[:130], 128, axis=1)
+    sub = (2.0 ** -9 if fmt == E4M3 else 2.0 ** -16) * sc
+    err = np.abs(xh - xf)
+    bf16_half_ulp = np.abs(xh) * 2.0 ** -8  # the final bf16 rounding (8 significant bits)
+    assert np.all(err <= u * np.abs(xf) + sub / 2 + bf16_half_ulp + 1e-45)
+
+
+def test_quantize_is_monotone_within_group():
+    x = synth.bf16_matrix(1, 4096, 1.0, 61)
+    order = np.argsort(_f32(x)[0], kind="stable")
+    for gran in (TENSOR, TOKEN):
+        q, s = oracle.quantize(x, E4M3, gran)
+        v = oracle.decode(q[0, order], E4M3)
+        assert np.all(np.diff(v) >= 0)
+
+
+def test_all_zero_group_gives_zero_codes_and_zero_scale():
+    x = np.zeros((4, 256), dtype=np.uint16)
+    x[1, :] = _bf16(np.linspace(-1, 1, 256))
+    for gran in (TOKEN, TILE_1x128):
+        q, s = oracle.quantize(x, E4M3, gran)
+        assert np.all(q[0] == 0) and np.all(q[2:] == 0)
+        assert s.reshape(-1)[0] == 0.0
+    q, sf = oracle.quantize(x, E4M3, MX32)
+    assert np.all(sf.reshape(4, 8)[0] == 0)  # e = -127 for an all-zero block
+
+
+def _underflow_rows():
+    rows = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "underflow_probe.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                mag, sc, err, fl = line.split()
+                rows[(float(mag), sc)] = (float(err), float(fl))
+    return rows
+
+
+def test_underflow_probe_from_guide():
+    rows = _underflow_rows()
+    rng = np.random.default_rng(77)
+    for mag in (1.0, 3e-4):
+        x = (rng.uniform(0.5, 1.5, 100000) * rng.choice([-1, 1], 100000) * mag).astype(np.float32)
+        xb = _bf16(x)
+        xf = _f32(xb).astype(np.float64)
+        # scale off: plain cast
+        q0, _ = oracle.quantize(xb.reshape(1, -1)[:, :99968], E4M3, TENSOR, static_scale=1.0)
+        # scale on: per-tensor current scaling
+        q1, s1 = oracle.quantize(xb.reshape(1, -1)[:, :99968], E4M3, TENSOR)
+        xs = xf[:99968]
+        for q, s, tag in ((q0, 1.0, "off"), (q1, float(s1[0]), "on")):
+            xh = oracle.decode(q[0], E4M3) * s
+            rel = np.mean(np.abs(xh - xs) / np.abs(xs)) * 100
+            flushed = np.mean(xh == 0) * 100
+            exp_err, exp_fl = rows[(mag, tag)]
+            assert abs(flushed - exp_fl) < 0.5, (mag, tag, flushed)
+            if exp_err >= 99:
+                assert rel == pytest.approx(100.0)
+            else:
+                assert 1.5 <= rel <= 3.0, (mag, tag, rel)  # the page prints ~2.1-2.2%
