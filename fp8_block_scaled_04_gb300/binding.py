@@ -1,0 +1,190 @@
+"""Thin ctypes binding over libfp8bs.so (argument marshalling only).
+
+Every computation runs in the library's CUDA kernels; torch supplies device
+memory (tensors) and the current stream. There is no CPU path: if the library
+is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfp8bs.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "fp8bs.h")
+
+E4M3, E5M2 = 0, 1
+TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32 = 0, 1, 2, 3, 4
+SF_LINEAR, SF_TCGEN05 = 0, 1
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+
+_lib = None
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s" % (what, status_string(code)))
+
+
+def lib():
+    """Load libfp8bs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfp8bs.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        i64, u64, i32, vp, sz = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        L.fp8_status_string.restype = ctypes.c_char_p
+        L.fp8_status_string.argtypes = [i32]
+        L.fp8_scales_bytes.restype = sz
+        L.fp8_scales_bytes.argtypes = [i64, i64, i32, i32]
+        L.fp8_quantize_workspace_bytes.restype = sz
+        L.fp8_quantize_workspace_bytes.argtypes = [i64, i64, i32]
+        L.fp8_quantize.restype = i32
+        L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, sz, vp]
+        L.fp8_dequantize.restype = i32
+        L.fp8_dequantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp]
+        L.fp8_gemm_blockscaled.restype = i32
+        L.fp8_gemm_blockscaled.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp, vp]
+        L.fp8_gemm_mx.restype = i32
+        L.fp8_gemm_mx.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
+        L.fp8_debug_encode_f32.restype = i32
+        L.fp8_debug_encode_f32.argtypes = [vp, i64, i32, vp, vp]
+        L.fp8_debug_wait_probe.restype = i32
+        L.fp8_debug_wait_probe.argtypes = [vp, u64, vp]
+        L.fp8_launch_count.restype = u64
+        L.fp8_launch_count.argtypes = []
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/fp8bs.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(code: int) -> str:
+    return lib().fp8_status_string(int(code)).decode()
+
+
+def launch_count() -> int:
+    return int(lib().fp8_launch_count())
+
+
+def scales_bytes(rows: int, cols: int, gran: int, sf_layout: int = SF_LINEAR) -> int:
+    return int(lib().fp8_scales_bytes(rows, cols, gran, sf_layout))
+
+
+def workspace_bytes(rows: int, cols: int, gran: int) -> int:
+    return int(lib().fp8_quantize_workspace_bytes(rows, cols, gran))
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise Fp8Error(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ---------------------------------------------------------------- quantize
+def quantize(x, fmt: int, gran: int, sf_layout: int = SF_LINEAR, static_scale=None, q=None, scales=None,
+             workspace=None, stream=None):
+    """x: bf16 CUDA tensor [rows, cols] (row stride may exceed cols).
+
+    Returns (q uint8 [rows, cols], scales) where scales is float32 (or uint8 for MX32).
+    """
+    import torch
+
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if scales is None:
+        nbytes = scales_bytes(rows, cols, gran, sf_layout)
+        if gran == MX32:
+            scales = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)[:nbytes]
+        else:
+            scales = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)[: nbytes // 4]
+    wsb = workspace_bytes(rows, cols, gran)
+    if workspace is None and wsb > 0 and static_scale is None:
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    rc = lib().fp8_quantize(_ptr(x), rows, cols, x.stride(0), fmt, gran, sf_layout, _ptr(static_scale), _ptr(q),
+                            q.stride(0), _ptr(scales), _ptr(workspace),
+                            0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "fp8_quantize")
+    return q, scales
+
+
+def dequantize(q, scales, fmt: int, gran: int, sf_layout: int = SF_LINEAR, out=None, stream=None):
+    import torch
+
+    assert q.dtype == torch.uint8 and q.dim() == 2 and q.stride(1) == 1
+    rows, cols = q.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
+    rc = lib().fp8_dequantize(_ptr(q), rows, cols, q.stride(0), fmt, gran, sf_layout, _ptr(scales), _ptr(out),
+                              out.stride(0), _stream(stream))
+    _check(rc, "fp8_dequantize")
+    return out
+
+
+# ---------------------------------------------------------------- GEMMs
+def gemm_blockscaled(a, a_scales, a_gran: int, b, b_scales, b_gran: int, a_fmt: int = E4M3, b_fmt: int = E4M3,
+                     out=None, status=None, stream=None):
+    """Out[M, N] bf16 = X_hat @ W_hat^T; a: uint8 [M, K], b: uint8 [N, K] (contiguous)."""
+    import torch
+
+    M, K = a.shape
+    N, K2 = b.shape
+    assert K == K2 and a.is_contiguous() and b.is_contiguous()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    rc = lib().fp8_gemm_blockscaled(_ptr(a), _ptr(a_scales), a_gran, _ptr(b), _ptr(b_scales), b_gran, a_fmt, b_fmt,
+                                    _ptr(out), M, N, K, _ptr(status), _stream(stream))
+    _check(rc, "fp8_gemm_blockscaled")
+    return out
+
+
+def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, status=None, stream=None):
+    """MXFP8 GEMM; a_sf / b_sf in the SF_TCGEN05 layout."""
+    import torch
+
+    M, K = a.shape
+    N, K2 = b.shape
+    assert K == K2 and a.is_contiguous() and b.is_contiguous()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    rc = lib().fp8_gemm_mx(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), a_fmt, b_fmt, _ptr(out), M, N, K,
+                           _ptr(status), _stream(stream))
+    _check(rc, "fp8_gemm_mx")
+    return out
+
+
+def debug_encode_f32(x, fmt: int, out=None, stream=None):
+    """RNE-satfinite encode of fp32 values (the quantizers' element step, scale 1)."""
+    import torch
+
+    assert x.dtype == torch.float32 and x.is_contiguous()
+    if out is None:
+        out = torch.empty(x.numel(), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_debug_encode_f32(_ptr(x), x.numel(), fmt, _ptr(out), _stream(stream)), "fp8_debug_encode_f32")
+    return out
+
+
+def debug_wait_probe(status, timeout_ns: int, stream=None):
+    _check(lib().fp8_debug_wait_probe(_ptr(status), int(timeout_ns), _stream(stream)), "fp8_debug_wait_probe")

@@ -1,0 +1,599 @@
+// gemm.cu -- scaled FP8 GEMMs on the sm_103a tensor cores (tcgen05 + TMA).
+//
+// Out[M x N] (bf16) = X[M x K] W[N x K]^T with FP8 operands and fp32
+// accumulation ("07 -- The FP8 Family", Scaling is what makes FP8 usable).
+// Three kernels share one warp-specialised, persistent structure:
+//   warp 0      TMA producer: operand tiles (and MX scale-factor atoms) into a
+//               ring of shared-memory stages;
+//   warp 1      tensor-memory owner and MMA issuer (one elected thread);
+//   warps 2..   consumers that read tensor memory with tcgen05.ld.
+//
+// gemm_fold_kernel -- 1x128 activation tiles x 128x128 weight blocks (the
+//   DeepSeek-V3 scheme of "07 -- The FP8 Family"; the promotion paragraph of
+//   "Low precision: FP8, FP4, and microscaling"). Each 128-wide K chunk is one
+//   MMA group into a fresh tensor-memory buffer; the consumer warps fold it
+//   into fp32 registers as acc += (s_x[m,kb] * s_w[n/128,kb]) * partial. Two
+//   tensor-memory buffers let the MMA of chunk kb+1 run while chunk kb folds.
+// gemm_tmem_kernel<false> -- per-tensor / per-token / per-channel scales: the
+//   whole K sum stays in tensor memory and the scale product is applied once
+//   in the epilogue.
+// gemm_tmem_kernel<true> -- MXFP8: kind::mxf8f6f4.block_scale applies one
+//   UE8M0 scale per 32 K-elements inside the tensor core ("Low precision",
+//   microscaling); scale-factor atoms go smem -> tensor memory with tcgen05.cp.
+//
+// Every barrier wait is bounded (see mbar_wait): on expiry the CTA records
+// FP8_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees tensor memory
+// and exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr int BM = 128;  // tile rows (MMA M)
+constexpr int BK = 128;  // K per stage (bytes of FP8)
+
+struct SharedCtl {
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void flag_abort(SharedCtl *ctl, int *dev_status) {
+  *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
+  if (dev_status != nullptr) atomicExch(dev_status, static_cast<int>(FP8_ERR_TIMEOUT));
+}
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+
+// Store 32 fp32 values (one row, 32 consecutive columns) as bf16; n_left is
+// the number of valid columns (multiple of 8).
+__device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32], int n_left) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (8 * j < n_left) {
+      uint4 w = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                           pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+      *reinterpret_cast<uint4 *>(dst + 8 * j) = w;
+    }
+  }
+}
+
+// Producer drain after an abort: wait (bounded) for the copies of the last
+// in-flight iterations so that no TMA write lands after the CTA exits.
+template <int STAGES>
+__device__ void drain_stages(uint64_t *full, int issued) {
+  const int first = issued > STAGES ? issued - STAGES : 0;
+  for (int j = first; j < issued; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1, kDrainTimeoutNs, nullptr);
+}
+
+// Tile order: consecutive CTAs walk down M inside one N band so that a band
+// of W stays hot in L2 while X tiles are re-read.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int &mt, int &nt) {
+  nt = tile / num_m;
+  mt = tile - nt * num_m;
+}
+
+// =====================================================================
+// Fold kernel: 1x128 x 128x128 scales, per-chunk fp32 fold in registers
+// =====================================================================
+template <int BN, int STAGES>
+struct FoldCfg {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int CONSUMER_WARPS = 4 * (BN / 128);  // each thread folds 128 columns of one row
+  static constexpr int THREADS = 64 + 32 * CONSUMER_WARPS;
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
+    gemm_fold_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out, int M,
+                     int N, int K, uint32_t idesc, int *dev_status) {
+  using C = FoldCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  __shared__ SharedCtl ctl;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = K / BK;
+  const int num_m = (M + BM - 1) / BM;
+  const int num_n = (N + BN - 1) / BN;
+  const int ntiles = num_m * num_n;
+  const int nblk128 = (N + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], C::CONSUMER_WARPS);
+    }
+    mbar_init(&drain, 1);
+    ctl.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, num_m, mt, nt);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t *a_s = smem + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(a_s, &tmA, kb * BK, mt * BM, &full[s]);
+          tma_load_2d(a_s + C::A_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+        }
+      }
+      if (!ok) {
+        flag_abort(&ctl, dev_status);
+        drain_stages<STAGES>(full, it);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, kc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+          const int b = kc & 1;
+          const int s = it % STAGES;
+          if (!mbar_wait(&tempty[b], ((kc >> 1) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
+              !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::A_BYTES;
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          tc_commit(&tfull[b]);
+        }
+      }
+      if (!ok) flag_abort(&ctl, dev_status);
+      tc_commit(&drain);
+      mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
+    }
+  } else {
+    // ------------------------------------------------ fold consumers
+    const int cw = warp - 2;
+    const int quarter = warp & 3;  // tensor-memory lanes this warp may access
+    const int half = cw >> 2;      // which 128-column half of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int kc = 0;
+    bool ok = true;
+    float acc[128];
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, num_m, mt, nt);
+      const int m = mt * BM + quarter * 32 + lane;
+      const bool row_ok = m < M;
+      const int nb = nt * (BN / 128) + half;
+      const bool col_ok = nb < nblk128;
+      const float *sa_row = sa + m;
+      const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      // scale prefetch, two chunks ahead
+      float sa0 = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb0 = col_ok ? __ldg(sb_blk) : 0.0f;
+      float sa1 = (row_ok && KB > 1) ? __ldg(sa_row + static_cast<int64_t>(M)) : 0.0f;
+      float sb1 = (col_ok && KB > 1) ? __ldg(sb_blk + 1) : 0.0f;
+      for (int kb = 0; kb < KB; ++kb, ++kc) {
+        const int b = kc & 1;
+        const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
+        const float sb2 = (col_ok && kb + 2 < KB) ? __ldg(sb_blk + kb + 2) : 0.0f;
+        const bool got = mbar_wait(&tfull[b], (kc >> 1) & 1, kWaitTimeoutNs, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sc = sa0 * sb0;
+        const uint32_t col = static_cast<uint32_t>(b * BN + half * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tmem + lane_base + col + 16 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(sc, __uint_as_float(r[i]), acc[16 * c + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        sa0 = sa1;
+        sb0 = sb1;
+        sa1 = sa2;
+        sb1 = sb2;
+      }
+      if (!ok) break;
+      // epilogue: bf16 out, straight from registers
+      if (row_ok) {
+        const int n0 = nb * 128;
+        uint16_t *dst = out + static_cast<int64_t>(m) * N + n0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = acc[32 * c + i];
+          store_row32(dst + 32 * c, v, N - n0 - 32 * c);
+        }
+      }
+    }
+    if (!ok && lane == 0) flag_abort(&ctl, dev_status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// =====================================================================
+// Tensor-memory accumulating kernel: epilogue-scaled (MX = false) or
+// block-scaled MXFP8 (MX = true)
+// =====================================================================
+template <bool MX, int BN, int STAGES>
+struct AccCfg {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int SFA_BYTES = MX ? 512 : 0;               // one 128x4 atom
+  static constexpr int SFB_BYTES = MX ? 512 * (BN / 128) : 0;  // BN/128 atoms
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
+  static constexpr int CONSUMER_WARPS = 4 * (BN / 128);
+  static constexpr int THREADS = 64 + 32 * CONSUMER_WARPS;
+  static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;  // tensor-memory columns per stage
+  static constexpr int ACC_COLS = 2 * BN;                       // two accumulators
+  static constexpr uint32_t TMEM_COLS = ACC_COLS + STAGES * SF_COLS <= 256 ? 256 : 512;
+  static constexpr int SMEM = STAGES * STAGE_STRIDE + 1024;
+  static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory budget");
+};
+
+template <bool MX, int BN, int STAGES>
+__global__ void __launch_bounds__(AccCfg<MX, BN, STAGES>::THREADS, 1)
+    gemm_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const float *__restrict__ sa, int sa_per_row, const float *__restrict__ sb, int sb_per_col,
+                     const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ out,
+                     int M, int N, int K, uint32_t idesc, int *dev_status) {
+  using C = AccCfg<MX, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  __shared__ uint64_t full[STAGES], empty[STAGES], afull[2], aempty[2], drain;
+  __shared__ SharedCtl ctl;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = (K + BK - 1) / BK;
+  const int num_m = (M + BM - 1) / BM;
+  const int num_n = (N + BN - 1) / BN;
+  const int ntiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], C::CONSUMER_WARPS);
+    }
+    mbar_init(&drain, 1);
+    ctl.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      const int nblk128_b = (N + 127) / 128;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, num_m, mt, nt);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = smem + s * C::STAGE_STRIDE;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(st, &tmA, kb * BK, mt * BM, &full[s]);
+          tma_load_2d(st + C::A_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+          if (MX) {
+            // scale-factor atoms: [row block][K/128 block] x 512 bytes
+            bulk_load(st + C::A_BYTES + C::B_BYTES, sfa + (static_cast<int64_t>(mt) * KB + kb) * 512, 512, &full[s]);
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j) {
+              int nb = nt * (BN / 128) + j;
+              nb = nb < nblk128_b ? nb : nblk128_b - 1;  // rows past N are zero; any finite scale will do
+              bulk_load(st + C::A_BYTES + C::B_BYTES + 512 + 512 * j,
+                        sfb + (static_cast<int64_t>(nb) * KB + kb) * 512, 512, &full[s]);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        flag_abort(&ctl, dev_status);
+        drain_stages<STAGES>(full, it);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      const uint32_t sf_col0 = static_cast<uint32_t>(C::ACC_COLS);
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tc) {
+        const int b = tc & 1;
+        if (!mbar_wait(&aempty[b], ((tc >> 1) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE_STRIDE);
+          const uint32_t b0 = a0 + C::A_BYTES;
+          if (MX) {
+            const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
+            const uint32_t sfb_t = sfa_t + 4;
+            const uint32_t sf_smem = b0 + C::B_BYTES;
+            tmem_cp_32x128b_warpx4(sfa_t, sdesc_plain_32x16(sf_smem));
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tmem_cp_32x128b_warpx4(sfb_t + 4 * j, sdesc_plain_32x16(sf_smem + 512 + 512 * j));
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              mma_mxf8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k),
+                           idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfa_t, sfb_t,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              mma_f8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc,
+                         (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&afull[b]);
+      }
+      if (!ok) flag_abort(&ctl, dev_status);
+      tc_commit(&drain);
+      mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
+    }
+  } else {
+    // ------------------------------------------------ epilogue consumers
+    const int cw = warp - 2;
+    const int quarter = warp & 3;
+    const int half = cw >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
+      int mt, nt;
+      tile_coords(tile, num_m, mt, nt);
+      const int b = tc & 1;
+      const int m = mt * BM + quarter * 32 + lane;
+      const bool row_ok = m < M;
+      const int n0 = nt * BN + half * 128;
+      const bool got = mbar_wait(&afull[b], (tc >> 1) & 1, kWaitTimeoutNs, &ctl.abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s_row = 1.0f;
+      if (!MX) s_row = row_ok ? __ldg(sa + (sa_per_row ? m : 0)) : 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(b * BN + half * 128 + 32 * c), r);
+        tmem_wait_ld();
+        if (c == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&aempty[b]);
+        }
+        const int nc = n0 + 32 * c;
+        if (row_ok && nc < N) {
+          float v[32];
+          if (MX) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          } else if (sb_per_col) {
+            const float4 *sbv = reinterpret_cast<const float4 *>(sb + nc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 q = (nc + 4 * i < N) ? __ldg(sbv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+              v[4 * i + 0] = __uint_as_float(r[4 * i + 0]) * (s_row * q.x);
+              v[4 * i + 1] = __uint_as_float(r[4 * i + 1]) * (s_row * q.y);
+              v[4 * i + 2] = __uint_as_float(r[4 * i + 2]) * (s_row * q.z);
+              v[4 * i + 3] = __uint_as_float(r[4 * i + 3]) * (s_row * q.w);
+            }
+          } else {
+            const float s = s_row * __ldg(sb);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * s;
+          }
+          store_row32(out + static_cast<int64_t>(m) * N + nc, v, N - nc);
+        }
+      }
+    }
+    if (!ok && lane == 0) flag_abort(&ctl, dev_status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// =====================================================================
+// Bounded-wait check: a barrier nothing ever arrives on
+// =====================================================================
+__global__ void wait_probe_kernel(int *dev_status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, timeout_ns, nullptr) && dev_status != nullptr)
+      atomicExch(dev_status, static_cast<int>(FP8_ERR_TIMEOUT));
+  }
+}
+
+// ------------------------------------------------------------------ host
+template <typename KernelT>
+bool ensure_smem(KernelT kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+int persistent_grid(int ntiles) {
+  const int sms = device_sm_count();
+  return ntiles < sms ? ntiles : sms;
+}
+
+}  // namespace
+
+fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+                              int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
+                              cudaStream_t stream) {
+  // Wide tiles when there are enough of them to fill the GPU, else 128-wide.
+  const int sms = device_sm_count();
+  const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+  const bool wide = tiles256 >= sms;
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, a, M, K, K, BM, BK)) return FP8_ERR_CUDA;
+  if (wide) {
+    constexpr int BN = 256, ST = 4;
+    using C = FoldCfg<BN, ST>;
+    if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
+    auto kern = gemm_fold_kernel<BN, ST>;
+    if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+    const int ntiles = static_cast<int>(tiles256);
+    kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
+        ta, tb, sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
+  } else {
+    constexpr int BN = 128, ST = 6;
+    using C = FoldCfg<BN, ST>;
+    if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
+    auto kern = gemm_fold_kernel<BN, ST>;
+    if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+    const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + 127) / 128));
+    kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
+        ta, tb, sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
+  }
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool a_token, const uint8_t *b,
+                                         const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,
+                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {
+  constexpr int BN = 256, ST = 4;
+  using C = AccCfg<false, BN, ST>;
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
+  auto kern = gemm_tmem_kernel<false, BN, ST>;
+  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+  const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
+  kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
+      ta, tb, sa, a_token ? 1 : 0, sb, b_token ? 1 : 0, nullptr, nullptr, out, static_cast<int>(M),
+      static_cast<int>(N), static_cast<int>(K), idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb, int a_fmt,
+                            int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
+                            cudaStream_t stream) {
+  constexpr int BN = 128, ST = 6;
+  using C = AccCfg<true, BN, ST>;
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
+  auto kern = gemm_tmem_kernel<true, BN, ST>;
+  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+  const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
+  kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
+      ta, tb, nullptr, 0, nullptr, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+      idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t launch_wait_probe(int *dev_status, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(dev_status, timeout_ns);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,54 @@
+// internal.h -- declarations shared by the translation units of libfp8bs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8bs.h"
+
+namespace fp8bs {
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+// Counts kernels enqueued by the library (diagnostic, see fp8_launch_count).
+void note_launches(int n);
+
+// Bounded-wait limit used by kernels (nanoseconds).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // 0.2 s for draining copies after an abort
+
+// ----------------------------------------------------------------- quantize
+fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, int gran,
+                             int sf_layout, const float *static_scale, uint8_t *q, int64_t ld_q, void *scales,
+                             void *workspace, cudaStream_t stream);
+
+fp8_status_t launch_encode_f32(const float *x, int64_t n, int fmt, uint8_t *out, cudaStream_t stream);
+
+fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, int fmt, int gran,
+                               int sf_layout, const void *scales, uint16_t *out, int64_t ld_out,
+                               cudaStream_t stream);
+
+// ----------------------------------------------------------------- GEMMs
+enum class EpiScale : int { kTensorTensor = 0, kTensorToken = 1, kTokenTensor = 2, kTokenToken = 3 };
+
+fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+                              int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
+                              cudaStream_t stream);
+
+fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool a_token, const uint8_t *b,
+                                         const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,
+                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream);
+
+fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb, int a_fmt,
+                            int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
+                            cudaStream_t stream);
+
+fp8_status_t launch_wait_probe(int *dev_status, uint64_t timeout_ns, cudaStream_t stream);
+
+// 2-D tensor map over a row-major uint8 matrix [rows x cols] (cols contiguous,
+// row stride ld bytes), box = box_cols x box_rows, 128-byte swizzle.
+bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                  uint32_t box_cols);
+
+}  // namespace fp8bs

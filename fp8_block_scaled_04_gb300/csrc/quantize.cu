@@ -1,0 +1,549 @@
+// quantize.cu -- bf16 -> FP8 quantizers (per-tensor two-pass, per-token,
+// 1x128 tile, 128x128 block, MX-32) and the FP8 -> bf16 dequantizer.
+//
+// Arithmetic follows "FP8 Mixed-Precision Serving in Production" (Quantization
+// Granularity and Scaling Topologies: s = max|X_group| / V_max) and the
+// qdq_e4m3 listing of "Low precision: FP8, FP4, and microscaling" (multiply
+// by 1/s, cvt.rn.satfinite, exact decode through f16, one fp32 multiply by s):
+//   s     = fp32_RN(amax / V_max)       (__fdiv_rn)
+//   s_inv = fp32_RN(1 / s), 0 if s == 0 or 1/s is not finite
+//   q     = RNE_satfinite(fp32_RN(x * s_inv))
+// MX-32 (microscaling paragraph of the same page): e = ceil(log2(fp32_RN(amax
+// / V_max))) clamped to [-127, 127], UE8M0 byte e + 127, q = RNE_satfinite(x * 2^-e).
+//
+// All kernels are bandwidth-bound streams: each warp reads whole 512-byte
+// lines with 16-byte loads (4 independent loads in flight per lane), reduces
+// the group amax with warp shuffles and writes the codes with 8-byte stores.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVecPerLane = 4;                   // 16-byte vectors in flight per lane
+constexpr int kSegVec = 32 * kVecPerLane;        // vectors a warp covers per task (1024 elements)
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float vmax_of(int fmt) { return fmt == FP8_E4M3 ? 448.0f : 57344.0f; }
+
+// max |x| of eight bf16 (as the 15-bit magnitude pattern, which orders like the value)
+__device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
+  const uint32_t m = 0x7fff7fffu;
+  uint32_t a = __vmaxu2(__vmaxu2(v.x & m, v.y & m), __vmaxu2(v.z & m, v.w & m));
+  return max(a & 0xffffu, a >> 16);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 v, float (&f)[8]) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xffff0000u);
+  f[4] = __uint_as_float(v.z << 16);
+  f[5] = __uint_as_float(v.z & 0xffff0000u);
+  f[6] = __uint_as_float(v.w << 16);
+  f[7] = __uint_as_float(v.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ void scale_pair(float amax, float vmax, float &s, float &s_inv) {
+  s = __fdiv_rn(amax, vmax);
+  s_inv = __frcp_rn(s);
+  if (s == 0.0f || !isfinite(s_inv)) s_inv = 0.0f;
+}
+
+// ceil(log2(fp32(amax / vmax))) from the bits, clamped to UE8M0's range.
+__device__ __forceinline__ int mx_shared_exponent(float amax, float vmax) {
+  const uint32_t u = __float_as_uint(__fdiv_rn(amax, vmax)) & 0x7fffffffu;
+  if (u == 0) return -127;
+  if (u >= 0x7f800000u) return 127;
+  const uint32_t ex = u >> 23, fr = u & 0x7fffffu;
+  int e;
+  if (ex != 0)
+    e = static_cast<int>(ex) - 127 + (fr != 0 ? 1 : 0);
+  else
+    e = (31 - __clz(fr)) - 149 + ((fr & (fr - 1u)) != 0 ? 1 : 0);
+  return min(127, max(-127, e));
+}
+
+// 2^p exactly, p in [-127, 127]
+__device__ __forceinline__ float exp2_exact(int p) {
+  return p >= -126 ? __uint_as_float(static_cast<uint32_t>(p + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s_inv) {
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(f[i], s_inv);
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = FMT == FP8_E4M3 ? cvt_e4m3x2(y[2 * i], y[2 * i + 1]) : cvt_e5m2x2(y[2 * i], y[2 * i + 1]);
+  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+__device__ __forceinline__ int64_t mx_tiled_index(int64_t r, int64_t j, int64_t ngroups) {
+  const int64_t col_blocks = (ngroups + 3) >> 2;
+  return (((r >> 7) * col_blocks + (j >> 2)) << 9) + ((r & 31) << 4) + (((r & 127) >> 5) << 2) + (j & 3);
+}
+
+// ------------------------------------------------------------ group kernels
+// GROUP elements share a scale (128: 1x128 tile, 32: MX). A warp task is one
+// row segment of kSegVec vectors; groups never straddle rows or lanes.
+template <int FMT, int GROUP, bool MX, bool TILED>
+__global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                               int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
+                                                               int64_t ldq, void *__restrict__ scales) {
+  constexpr int TPG = GROUP / 8;
+  const int lane = threadIdx.x & 31;
+  const int64_t vec_per_row = cols >> 3;
+  const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
+  const int64_t tasks = rows * segs;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const float vmax = vmax_of(FMT);
+  for (int64_t t = warp0; t < tasks; t += nwarps) {
+    const int64_t r = t / segs;
+    const int64_t cv0 = (t - r * segs) * kSegVec;
+    uint4 v[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      v[i] = cv < vec_per_row ? ld_stream_v4(x + r * ldx + cv * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      uint32_t m = absmax_bits8(v[i]);
+#pragma unroll
+      for (int o = TPG / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float amax = __uint_as_float(m << 16);
+      if (cv >= vec_per_row) continue;
+      float f[8];
+      bf16x8_to_f32(v[i], f);
+      float s_inv;
+      if (MX) {
+        const int e = mx_shared_exponent(amax, vmax);
+        s_inv = exp2_exact(-e);
+        if ((lane & (TPG - 1)) == 0) {
+          const int64_t j = cv / TPG;
+          const int64_t ng = cols / 32;
+          uint8_t *sf = static_cast<uint8_t *>(scales);
+          sf[TILED ? mx_tiled_index(r, j, ng) : r * ng + j] = static_cast<uint8_t>(e + 127);
+        }
+      } else {
+        float s;
+        scale_pair(amax, vmax, s, s_inv);
+        if ((lane & (TPG - 1)) == 0) static_cast<float *>(scales)[(cv / TPG) * rows + r] = s;
+      }
+      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+    }
+  }
+}
+
+// ------------------------------------------------------------ per-tensor
+// Pass 1: grid-wide amax. Non-negative floats order like their bit patterns,
+// so the reduction is an unsigned atomicMax on the fp32 bits.
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                        int64_t ldx, uint32_t *__restrict__ amax_bits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t vec_per_row = cols >> 3;
+  const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
+  const int64_t tasks = rows * segs;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  uint32_t m = 0;
+  for (int64_t t = warp0; t < tasks; t += nwarps) {
+    const int64_t r = t / segs;
+    const int64_t cv0 = (t - r * segs) * kSegVec;
+    uint4 v[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      v[i] = cv < vec_per_row ? ld_stream_v4(x + r * ldx + cv * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) m = max(m, absmax_bits8(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[kThreads / 32];
+  if (lane == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
+    atomicMax(amax_bits, b << 16);
+  }
+}
+
+// Pass 2: encode with one scale; the scale comes from the amax of pass 1 or
+// from the caller (static scaling).
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) quant_tensor_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
+                                                                int64_t ldq, float *__restrict__ scale_out,
+                                                                const uint32_t *__restrict__ amax_bits,
+                                                                const float *__restrict__ static_scale) {
+  float s, s_inv;
+  if (static_scale != nullptr) {
+    s = *static_scale;
+    s_inv = __frcp_rn(s);
+    if (s == 0.0f || !isfinite(s_inv)) s_inv = 0.0f;
+  } else {
+    scale_pair(__uint_as_float(*amax_bits), vmax_of(FMT), s, s_inv);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  const int lane = threadIdx.x & 31;
+  const int64_t vec_per_row = cols >> 3;
+  const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
+  const int64_t tasks = rows * segs;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  for (int64_t t = warp0; t < tasks; t += nwarps) {
+    const int64_t r = t / segs;
+    const int64_t cv0 = (t - r * segs) * kSegVec;
+    uint4 v[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      v[i] = cv < vec_per_row ? ld_stream_v4(x + r * ldx + cv * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      if (cv >= vec_per_row) continue;
+      float f[8];
+      bf16x8_to_f32(v[i], f);
+      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+    }
+  }
+}
+
+// ------------------------------------------------------------ per-token
+// One CTA per row; the row stays in registers between the amax reduction and
+// the encode (U vectors per thread, rows up to 256 * U * 8 elements).
+template <int FMT, int U>
+__global__ void __launch_bounds__(kThreads) quant_token_kernel(const uint16_t *__restrict__ x, int64_t cols,
+                                                               int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                                                               float *__restrict__ scales) {
+  const int64_t r = blockIdx.x;
+  const int64_t vec_per_row = cols >> 3;
+  const uint16_t *xr = x + r * ldx;
+  uint4 v[U];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    const int64_t cv = threadIdx.x + static_cast<int64_t>(i) * kThreads;
+    v[i] = cv < vec_per_row ? ld_stream_v4(xr + cv * 8) : make_uint4(0, 0, 0, 0);
+    m = max(m, absmax_bits8(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  uint32_t b = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
+  float s, s_inv;
+  scale_pair(__uint_as_float(b << 16), vmax_of(FMT), s, s_inv);
+  if (threadIdx.x == 0) scales[r] = s;
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    const int64_t cv = threadIdx.x + static_cast<int64_t>(i) * kThreads;
+    if (cv < vec_per_row) {
+      float f[8];
+      bf16x8_to_f32(v[i], f);
+      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+    }
+  }
+}
+
+// Rows longer than the register-resident kernel handles: amax loop, then an
+// encode loop that re-reads the row (mostly from L2).
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) quant_token_long_kernel(const uint16_t *__restrict__ x, int64_t cols,
+                                                                    int64_t ldx, uint8_t *__restrict__ q,
+                                                                    int64_t ldq, float *__restrict__ scales) {
+  const int64_t r = blockIdx.x;
+  const int64_t vec_per_row = cols >> 3;
+  const uint16_t *xr = x + r * ldx;
+  uint32_t m = 0;
+  for (int64_t cv = threadIdx.x; cv < vec_per_row; cv += kThreads) m = max(m, absmax_bits8(ld_stream_v4(xr + cv * 8)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  uint32_t b = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
+  float s, s_inv;
+  scale_pair(__uint_as_float(b << 16), vmax_of(FMT), s, s_inv);
+  if (threadIdx.x == 0) scales[r] = s;
+  for (int64_t cv = threadIdx.x; cv < vec_per_row; cv += kThreads) {
+    float f[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + cv * 8), f);
+    *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+  }
+}
+
+// ------------------------------------------------------------ 128x128 blocks
+// One CTA per block: thread t holds column vector t%16 of rows t/16 + 16*i.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) quant_block_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                               int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
+                                                               int64_t ldq, float *__restrict__ scales) {
+  const int64_t kb = blockIdx.x, rb = blockIdx.y;
+  const int cvl = threadIdx.x & 15;
+  const int r0 = threadIdx.x >> 4;
+  uint4 v[8];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = rb * 128 + r0 + 16 * i;
+    v[i] = r < rows ? ld_stream_v4(x + r * ldx + kb * 128 + cvl * 8) : make_uint4(0, 0, 0, 0);
+    m = max(m, absmax_bits8(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  uint32_t b = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
+  float s, s_inv;
+  scale_pair(__uint_as_float(b << 16), vmax_of(FMT), s, s_inv);
+  if (threadIdx.x == 0) scales[rb * (cols / 128) + kb] = s;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = rb * 128 + r0 + 16 * i;
+    if (r < rows) {
+      float f[8];
+      bf16x8_to_f32(v[i], f);
+      *reinterpret_cast<uint2 *>(q + r * ldq + kb * 128 + cvl * 8) = encode8<FMT>(f, s_inv);
+    }
+  }
+}
+
+// ------------------------------------------------------------ dequantize
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__restrict__ q, int64_t rows, int64_t cols,
+                                                           int64_t ldq, int gran, int sf_layout,
+                                                           const void *__restrict__ scales,
+                                                           uint16_t *__restrict__ out, int64_t ldo) {
+  const int lane = threadIdx.x & 31;
+  const int64_t vec_per_row = cols >> 4;  // 16 codes per vector
+  const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
+  const int64_t tasks = rows * segs;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const float *sf = static_cast<const float *>(scales);
+  const uint8_t *sb = static_cast<const uint8_t *>(scales);
+  for (int64_t t = warp0; t < tasks; t += nwarps) {
+    const int64_t r = t / segs;
+    const int64_t cv0 = (t - r * segs) * kSegVec;
+    uint4 v[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      v[i] = cv < vec_per_row ? ld_stream_v4(q + r * ldq + cv * 16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const int64_t cv = cv0 + i * 32 + lane;
+      if (cv >= vec_per_row) continue;
+      const int64_t c = cv * 16;
+      float s;
+      switch (gran) {
+        case FP8_GRAN_TENSOR: s = sf[0]; break;
+        case FP8_GRAN_TOKEN: s = sf[r]; break;
+        case FP8_GRAN_TILE_1x128: s = sf[(c >> 7) * rows + r]; break;
+        case FP8_GRAN_BLOCK_128x128: s = sf[(r >> 7) * (cols >> 7) + (c >> 7)]; break;
+        default: {
+          const int64_t ng = cols >> 5;
+          const uint8_t e = sb[sf_layout == FP8_SF_TCGEN05 ? mx_tiled_index(r, c >> 5, ng) : r * ng + (c >> 5)];
+          s = e == 0xff ? __uint_as_float(0x7fc00000u) : exp2_exact(static_cast<int>(e) - 127);
+        }
+      }
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint16_t pair = static_cast<uint16_t>(w[j] >> (16 * h));
+          const uint32_t hx2 = FMT == FP8_E4M3 ? cvt_e4m3x2_to_f16x2(pair) : cvt_e5m2x2_to_f16x2(pair);
+          const __half2 hh = *reinterpret_cast<const __half2 *>(&hx2);
+          const float lo = __fmul_rn(__low2float(hh), s);
+          const float hi = __fmul_rn(__high2float(hh), s);
+          const uint32_t blo = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+          const uint32_t bhi = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+          o[2 * j + h] = blo | (bhi << 16);
+        }
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(out + r * ldo + c);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// ------------------------------------------------------------ codec check
+// Encodes fp32 inputs with the quantizers' element step (scale 1), so every
+// fp32 bit pattern can be checked against the reference codec.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) encode_f32_kernel(const float *__restrict__ x, int64_t n8,
+                                                              uint8_t *__restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const float4 a = reinterpret_cast<const float4 *>(x)[2 * i];
+    const float4 b = reinterpret_cast<const float4 *>(x)[2 * i + 1];
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    reinterpret_cast<uint2 *>(out)[i] = encode8<FMT>(f, 1.0f);
+  }
+}
+
+int stream_grid(int64_t tasks) {
+  // 8 resident CTAs of 256 threads per SM; never more CTAs than warp tasks need
+  const int64_t full = static_cast<int64_t>(device_sm_count()) * 8;
+  const int64_t need = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
+  return static_cast<int>(need < full ? (need > 0 ? need : 1) : full);
+}
+
+}  // namespace
+
+fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, int gran,
+                             int sf_layout, const float *static_scale, uint8_t *q, int64_t ld_q, void *scales,
+                             void *workspace, cudaStream_t stream) {
+  const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
+  const int grid = stream_grid(tasks);
+  const bool e4 = fmt == FP8_E4M3;
+  int launches = 0;
+  switch (gran) {
+    case FP8_GRAN_TENSOR: {
+      uint32_t *amax = static_cast<uint32_t *>(workspace);
+      if (static_scale == nullptr) {
+        if (cudaMemsetAsync(amax, 0, sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
+        amax_kernel<<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, amax);
+        ++launches;
+      }
+      if (e4)
+        quant_tensor_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
+                                                                     static_cast<float *>(scales), amax, static_scale);
+      else
+        quant_tensor_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
+                                                                     static_cast<float *>(scales), amax, static_scale);
+      ++launches;
+      break;
+    }
+    case FP8_GRAN_TOKEN: {
+      const int64_t vec = cols / 8;
+      float *s = static_cast<float *>(scales);
+      const unsigned nb = static_cast<unsigned>(rows);
+#define FP8BS_TOKEN(U)                                                                         \
+  (e4 ? (quant_token_kernel<FP8_E4M3, U><<<nb, kThreads, 0, stream>>>(x, cols, ld_x, q, ld_q, s)) \
+      : (quant_token_kernel<FP8_E5M2, U><<<nb, kThreads, 0, stream>>>(x, cols, ld_x, q, ld_q, s)))
+      if (vec <= kThreads)
+        FP8BS_TOKEN(1);
+      else if (vec <= 2 * kThreads)
+        FP8BS_TOKEN(2);
+      else if (vec <= 4 * kThreads)
+        FP8BS_TOKEN(4);
+      else if (vec <= 8 * kThreads)
+        FP8BS_TOKEN(8);
+      else if (e4)
+        quant_token_long_kernel<FP8_E4M3><<<nb, kThreads, 0, stream>>>(x, cols, ld_x, q, ld_q, s);
+      else
+        quant_token_long_kernel<FP8_E5M2><<<nb, kThreads, 0, stream>>>(x, cols, ld_x, q, ld_q, s);
+#undef FP8BS_TOKEN
+      ++launches;
+      break;
+    }
+    case FP8_GRAN_TILE_1x128:
+      if (e4)
+        quant_group_kernel<FP8_E4M3, 128, false, false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
+                                                                                     scales);
+      else
+        quant_group_kernel<FP8_E5M2, 128, false, false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
+                                                                                     scales);
+      ++launches;
+      break;
+    case FP8_GRAN_BLOCK_128x128: {
+      dim3 g(static_cast<unsigned>(cols / 128), static_cast<unsigned>((rows + 127) / 128));
+      if (e4)
+        quant_block_kernel<FP8_E4M3><<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
+                                                                 static_cast<float *>(scales));
+      else
+        quant_block_kernel<FP8_E5M2><<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
+                                                                 static_cast<float *>(scales));
+      ++launches;
+      break;
+    }
+    case FP8_GRAN_MX32: {
+      const bool tiled = sf_layout == FP8_SF_TCGEN05;
+      if (tiled && (rows % 128 != 0 || cols % 128 != 0)) {
+        const size_t bytes = static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) * 512;
+        if (cudaMemsetAsync(scales, 0, bytes, stream) != cudaSuccess) return FP8_ERR_CUDA;
+      }
+#define FP8BS_MX(F, T) \
+  quant_group_kernel<F, 32, true, T><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales)
+      if (e4 && tiled)
+        FP8BS_MX(FP8_E4M3, true);
+      else if (e4)
+        FP8BS_MX(FP8_E4M3, false);
+      else if (tiled)
+        FP8BS_MX(FP8_E5M2, true);
+      else
+        FP8BS_MX(FP8_E5M2, false);
+#undef FP8BS_MX
+      ++launches;
+      break;
+    }
+    default:
+      return FP8_ERR_INVALID_ARG;
+  }
+  note_launches(launches);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t launch_encode_f32(const float *x, int64_t n, int fmt, uint8_t *out, cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  const int grid = stream_grid((n8 + 31) / 32);
+  if (fmt == FP8_E4M3)
+    encode_f32_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, n8, out);
+  else
+    encode_f32_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, n8, out);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, int fmt, int gran,
+                               int sf_layout, const void *scales, uint16_t *out, int64_t ld_out,
+                               cudaStream_t stream) {
+  const int64_t tasks = rows * ((cols / 16 + kSegVec - 1) / kSegVec);
+  const int grid = stream_grid(tasks);
+  if (fmt == FP8_E4M3)
+    dequant_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
+  else
+    dequant_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace fp8bs

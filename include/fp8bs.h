@@ -1,0 +1,189 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs.so: FP8 quantization and scaled FP8 GEMM on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (page title, section):
+ *   "07 -- The FP8 Family: E4M3, E5M2, and Per-Block Scaling" ("The two
+ *       shapes", "Scaling is what makes FP8 usable", "The scaling granularity
+ *       ladder", "DeepSeek-V3: fp8 training in the wild");
+ *   "FP8 Mixed-Precision Serving in Production ..." ("The Mathematics of FP8",
+ *       "Quantization Granularity and Scaling Topologies", "Engineering
+ *       Trade-Offs and Best Practices");
+ *   "Low precision: FP8, FP4, and microscaling" (qdq_e4m3 listing,
+ *       microscaling paragraphs, DeepSeek-V3 promotion paragraph).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers named *_dev are DEVICE pointers owned by the caller. The
+ *     library never allocates, frees or synchronises; it enqueues kernels on
+ *     `stream` (NULL = the legacy default stream) and returns.
+ *   - Matrices are row-major. bf16 and fp8 elements are stored as raw bit
+ *     patterns (uint16 / uint8). A GEMM operand pair is X [M x K] and
+ *     W [N x K], both K-contiguous ("TN"); the output is Out = X W^T [M x N]
+ *     bf16, row-major with leading dimension N.
+ *   - Argument checks run on the host before any launch; a failed check
+ *     returns a non-zero fp8_status_t and enqueues nothing. A CUDA error at
+ *     launch returns FP8_ERR_CUDA. Every wait inside a kernel is bounded: on
+ *     expiry the kernel stores FP8_ERR_TIMEOUT into *dev_status (when
+ *     non-NULL), drains its own copies in flight, frees its tensor memory and
+ *     returns; the caller zeroes *dev_status beforehand and reads it after the
+ *     stream completes. The library writes *dev_status only on error.
+ *   - An empty problem (a zero dimension) is valid and enqueues nothing.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *fp8_stream_t;
+
+/* FP8 element formats ("07 -- The FP8 Family", format table and bit layout).
+ * E4M3: bias 7, max 448, no infinities, NaN = S1111111.
+ * E5M2: bias 15, max 57344, IEEE infinities and NaNs. */
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
+
+/* Scaling granularity ("07 -- The FP8 Family", scaling granularity ladder;
+ * "FP8 Mixed-Precision Serving", Quantization Granularity and Scaling
+ * Topologies). Scale arrays, for an operand of [rows x cols]:
+ *   TENSOR         float[1]
+ *   TOKEN          float[rows]                      (one per row)
+ *   TILE_1x128     float[cols/128][rows]            (rows contiguous)
+ *   BLOCK_128x128  float[ceil(rows/128)][cols/128]
+ *   MX32           uint8 UE8M0 (2^(b-127)), one per 32 consecutive elements
+ *                  of a row, in the layout chosen by fp8_sf_layout_t. */
+typedef enum {
+  FP8_GRAN_TENSOR = 0,
+  FP8_GRAN_TOKEN = 1,
+  FP8_GRAN_TILE_1x128 = 2,
+  FP8_GRAN_BLOCK_128x128 = 3,
+  FP8_GRAN_MX32 = 4
+} fp8_gran_t;
+
+/* MX scale-factor layouts.
+ *   LINEAR   uint8[rows][cols/32].
+ *   TCGEN05  the tiled layout the tensor-core block-scaled MMA consumes
+ *            ("Low precision", microscaling: "a scale-factor tensor in its
+ *            required tiled layout"): rows cut into blocks of 128, the
+ *            32-element groups into blocks of 4; each 128x4 block is 512
+ *            bytes, blocks row-block-major; inside a block the byte of
+ *            (row r, group j) is at (r%32)*16 + ((r%128)/32)*4 + (j%4).
+ *            Size: ceil(rows/128) * ceil(cols/128) * 512 bytes; padding bytes
+ *            are written as 0. */
+typedef enum { FP8_SF_LINEAR = 0, FP8_SF_TCGEN05 = 1 } fp8_sf_layout_t;
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, bad combination      */
+  FP8_ERR_ALIGNMENT = 2,         /* pointer or leading dimension misaligned      */
+  FP8_ERR_UNSUPPORTED_SHAPE = 3, /* dimension rule violated (no fallback path)   */
+  FP8_ERR_WORKSPACE = 4,         /* workspace missing or too small               */
+  FP8_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed            */
+  FP8_ERR_TIMEOUT = 6            /* written to *dev_status by an expired wait    */
+} fp8_status_t;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *fp8_status_string(fp8_status_t status);
+
+/* Bytes of the scale array fp8_quantize writes for this shape, or 0 for an
+ * invalid combination. */
+size_t fp8_scales_bytes(int64_t rows, int64_t cols, fp8_gran_t gran, fp8_sf_layout_t sf_layout);
+
+/* Workspace bytes fp8_quantize needs: 256 for dynamic per-tensor scaling (the
+ * grid-wide amax of the first pass lives there), 0 otherwise. */
+size_t fp8_quantize_workspace_bytes(int64_t rows, int64_t cols, fp8_gran_t gran);
+
+/* Dynamic (or static per-tensor) quantization of a bf16 matrix.
+ *   "07 -- The FP8 Family", Scaling is what makes FP8 usable: x_fp8 =
+ *   clip(round(x/s)); "FP8 Mixed-Precision Serving", per-tensor static, current
+ *   scaling and block-wise scaling: s = max|X_group| / V_max; "Low precision",
+ *   qdq_e4m3 listing: multiply by 1/s, round to nearest even, saturate.
+ * Per group: amax = max |x|; s = fp32(amax / V_max) with V_max = 448 (E4M3) or
+ * 57344 (E5M2); s_inv = fp32(1 / s), replaced by 0 when s == 0 or 1/s is not
+ * finite; q = RNE_satfinite(fp32(x * s_inv)). MX32: e = ceil(log2(fp32(amax /
+ * V_max))) clamped to [-127, 127] (-127 for amax 0), byte = e + 127, q =
+ * RNE_satfinite(x * 2^-e). TENSOR with static_scale_dev != NULL uses s =
+ * *static_scale_dev (calibrated scaling) and copies it to scales_out.
+ *   x_dev        bf16 [rows x cols], leading dimension ld_x (elements)
+ *   q_dev        fp8 out [rows x cols], leading dimension ld_q (bytes)
+ *   scales_dev   out, fp8_scales_bytes(rows, cols, gran, sf_layout) bytes
+ *   workspace    device scratch of fp8_quantize_workspace_bytes() bytes
+ *                (may be NULL when that is 0); its contents are clobbered;
+ *                concurrent calls must not share it.
+ * Shape rules: cols % 16 == 0 (TENSOR, TOKEN), cols % 128 == 0 (TILE_1x128,
+ * BLOCK_128x128), cols % 32 == 0 (MX32). x_dev and q_dev 16-byte aligned,
+ * ld_x % 8 == 0, ld_q % 16 == 0, scales_dev 4-byte aligned. */
+fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x, fp8_format_t fmt,
+                          fp8_gran_t gran, fp8_sf_layout_t sf_layout, const float *static_scale_dev, void *q_dev,
+                          int64_t ld_q, void *scales_dev, void *workspace_dev, size_t workspace_bytes,
+                          fp8_stream_t stream);
+
+/* Dequantization ("07 -- The FP8 Family": x_hat = x_fp8 * s; "Low precision",
+ * qdq_e4m3 listing: exact decode, then one fp32 multiply by s):
+ * out = bf16_RN(fp32(decode(q) * s)). Same layouts and rules as fp8_quantize;
+ * out_dev bf16 [rows x cols] with leading dimension ld_out (elements, % 8). */
+fp8_status_t fp8_dequantize(const void *q_dev, int64_t rows, int64_t cols, int64_t ld_q, fp8_format_t fmt,
+                            fp8_gran_t gran, fp8_sf_layout_t sf_layout, const void *scales_dev, void *out_dev,
+                            int64_t ld_out, fp8_stream_t stream);
+
+/* Scaled FP8 GEMM with fp32 accumulation and bf16 output
+ * ("07 -- The FP8 Family", Scaling is what makes FP8 usable:
+ *  Out = (X_fp8 s_X)(W_fp8 s_W)^T = s_X s_W (X_fp8 W_fp8^T) in fp32).
+ * Valid (a_gran, b_gran) pairs:
+ *   (TILE_1x128, BLOCK_128x128)  DeepSeek-V3 fine-grained scaling ("07 -- The
+ *       FP8 Family", DeepSeek-V3 callout; "Low precision", promotion paragraph):
+ *       every 128-wide K chunk's tensor-core partial is multiplied by
+ *       s_X[m, kb] * s_W[n/128, kb] and added to an fp32 accumulator. K % 128 == 0.
+ *   (TENSOR | TOKEN, TENSOR | TOKEN)  per-tensor, per-token activation and
+ *       per-channel weight scales (TOKEN on W = one scale per output column):
+ *       the whole K sum accumulates in the tensor core and the scale product is
+ *       applied once in the epilogue. K % 16 == 0.
+ * a_dev: X fp8 [M x K]; b_dev: W fp8 [N x K]; out_dev: bf16 [M x N].
+ * Rules: M >= 1, N % 16 == 0 ("FP8 Mixed-Precision Serving", hardware-aligned
+ * sizing: multiples of 16, no slower fallback), M, N, K < 2^31; a_dev, b_dev,
+ * out_dev 16-byte aligned; scales 4-byte aligned. a_fmt / b_fmt may differ.
+ * dev_status: NULL or a device int (see conventions). */
+fp8_status_t fp8_gemm_blockscaled(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,
+                                  const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
+                                  fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N,
+                                  int64_t K, int *dev_status, fp8_stream_t stream);
+
+/* MXFP8 GEMM on the tensor core's block-scaled MMA ("Low precision",
+ * microscaling: 32 consecutive elements share one UE8M0 scale, applied inside
+ * the tensor core). Out[m][n] = sum_k decode(a[m][k]) 2^(sfa(m,k/32)-127)
+ * decode(b[n][k]) 2^(sfb(n,k/32)-127), fp32 accumulation over all of K, bf16
+ * out. a_sf_dev / b_sf_dev are in the FP8_SF_TCGEN05 layout for [M x K] and
+ * [N x K]. Rules: K % 32 == 0, N % 16 == 0, M >= 1, alignment as above. */
+fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
+                         fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
+                         int *dev_status, fp8_stream_t stream);
+
+/* Codec check (no counterpart on the pages beyond the element step itself):
+ * out[i] = RNE_satfinite(x[i]) in `fmt`, computed by the same device routine
+ * the quantizers use for their last step ("Low precision", qdq_e4m3 listing:
+ * cvt.rn.satfinite), so that every fp32 input can be compared with a
+ * reference encoder. x_dev fp32 [n] (16-byte aligned), out_dev uint8 [n]
+ * (8-byte aligned), n % 8 == 0. */
+fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fmt, void *out_dev,
+                                  fp8_stream_t stream);
+
+/* Check of the bounded-wait machinery the GEMM kernels use (no counterpart on
+ * the pages): launches one CTA that waits on a barrier nothing ever arrives
+ * on, with a limit of timeout_ns nanoseconds; on expiry the kernel stores
+ * FP8_ERR_TIMEOUT into *dev_status and returns, leaving the context usable.
+ * timeout_ns must be in (0, 10^10]. */
+fp8_status_t fp8_debug_wait_probe(int *dev_status, uint64_t timeout_ns, fp8_stream_t stream);
+
+/* Number of kernel launches the library has enqueued since it was loaded
+ * (all entry points, all devices); a diagnostic counter. */
+uint64_t fp8_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,167 @@
+"""GPU parity of the scaled FP8 GEMMs against the CPU oracle.
+
+Tolerance (fixed before any kernel ran): |gpu - ref| <= 1e-3 * sum_k |x_hat w_hat| + 1e-6
+element-wise, with ref the fp64 sum over dequantized operands. Small-integer
+operands with power-of-two scales must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_04_gb300 import binding as fb
+from fp8_block_scaled_04_gb300 import synth
+from gpu_util import out_f64, to_dev_bf16, within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant_pair(x, w, ga, gb, fa=fb.E4M3, fw=fb.E4M3, layout=fb.SF_LINEAR):
+    """Operands quantized by the oracle (CPU) so the GEMM is tested on its own."""
+    qa, sa = oracle.quantize(x, fa, ga, layout)
+    qb, sb = oracle.quantize(w, fw, gb, layout)
+    return qa, sa, qb, sb
+
+
+def _run_blockscaled(qa, sa, ga, qb, sb, gb, fa=fb.E4M3, fw=fb.E4M3):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = fb.gemm_blockscaled(torch.from_numpy(qa).cuda(), torch.from_numpy(sa).cuda(), ga,
+                              torch.from_numpy(qb).cuda(), torch.from_numpy(sb).cuda(), gb, fa, fw, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+def _run_mx(qa, sfa, qb, sfb, fa=fb.E4M3, fw=fb.E4M3):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = fb.gemm_mx(torch.from_numpy(qa).cuda(), torch.from_numpy(sfa).cuda(), torch.from_numpy(qb).cuda(),
+                     torch.from_numpy(sfb).cuda(), fa, fw, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+def test_tiny_config_blockscaled():
+    x, w = synth.tiny()
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    bad, worst = within_tolerance(out_f64(out), ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (17, 48, 256), (130, 272, 640), (300, 384, 384),
+                                   (257, 512, 1152), (128, 4096, 256), (640, 1280, 512)])
+def test_fold_ragged_shapes(M, N, K):
+    x = synth.bf16_matrix(M, K, 1.0, 10 + M, 20 + K, 0.01, 50.0)
+    w = synth.bf16_matrix(N, K, 0.02, 30 + N)
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    bad, worst = within_tolerance(out_f64(out), ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+def test_fold_small_integers_exact():
+    """Integer-valued FP8 operands, power-of-two scales, K <= 512: fp32 sums are exact."""
+    rng = np.random.default_rng(1)
+    M, N, K = 130, 272, 512
+    a = oracle.encode(rng.integers(-8, 9, (M, K)).astype(np.float32), fb.E4M3)
+    b = oracle.encode(rng.integers(-8, 9, (N, K)).astype(np.float32), fb.E4M3)
+    sa = (2.0 ** rng.integers(-3, 4, (K // 128) * M)).astype(np.float32)
+    sb = (2.0 ** rng.integers(-3, 4, ((N + 127) // 128) * (K // 128))).astype(np.float32)
+    out = _run_blockscaled(a, sa, fb.TILE_1x128, b, sb, fb.BLOCK_128x128)
+    ref, _ = oracle.gemm(a, sa, fb.TILE_1x128, b, sb, fb.BLOCK_128x128)
+    expect = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(out_f64(out), expect)
+
+
+@pytest.mark.parametrize("fa,fw", [(fb.E5M2, fb.E4M3), (fb.E4M3, fb.E5M2), (fb.E5M2, fb.E5M2)])
+def test_fold_e5m2_operands(fa, fw):
+    x, w = synth.tiny()
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128, fa, fw)
+    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, fa, fw)
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, fa, fw)
+    bad, worst = within_tolerance(out_f64(out), ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+@pytest.mark.parametrize("ga,gb", [(fb.TENSOR, fb.TENSOR), (fb.TOKEN, fb.TOKEN), (fb.TOKEN, fb.TENSOR),
+                                   (fb.TENSOR, fb.TOKEN)])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 144), (130, 272, 400), (300, 512, 1024)])
+def test_epilogue_scaled_modes(ga, gb, M, N, K):
+    x = synth.bf16_matrix(M, K, 1.0, 40 + M, 41, 0.01, 30.0)
+    w = synth.bf16_matrix(N, K, 0.02, 42 + N)
+    qa, sa, qb, sb = _quant_pair(x, w, ga, gb)
+    out = _run_blockscaled(qa, sa, ga, qb, sb, gb)
+    ref, bound = oracle.gemm(qa, sa, ga, qb, sb, gb)
+    bad, worst = within_tolerance(out_f64(out), ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+def test_uniform_block_scales_match_per_tensor_path():
+    x, w = synth.tiny()
+    qa, _ = oracle.quantize(x, fb.E4M3, fb.TENSOR)
+    qb, _ = oracle.quantize(w, fb.E4M3, fb.TENSOR)
+    sa = np.full(4 * 128, 0.5, np.float32)
+    sb = np.full(2 * 4, 0.25, np.float32)
+    o1 = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    o2 = _run_blockscaled(qa, np.array([0.5], np.float32), fb.TENSOR, qb, np.array([0.25], np.float32), fb.TENSOR)
+    ref, bound = oracle.gemm(qa, np.array([0.5], np.float32), fb.TENSOR, qb, np.array([0.25], np.float32), fb.TENSOR)
+    assert within_tolerance(out_f64(o1), ref, bound)[0] == 0
+    assert within_tolerance(out_f64(o2), ref, bound)[0] == 0
+
+
+# ------------------------------------------------------------------ MX
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 256, 512), (130, 272, 416), (1, 16, 32), (300, 640, 1024)])
+def test_mx_shapes(M, N, K):
+    x = synth.bf16_matrix(M, K, 1.0, 50 + M, 51, 0.005, 50.0)
+    w = synth.bf16_matrix(N, K, 1.0, 52 + N, 53, 0.005, 50.0)
+    qa, sfa, qb, sfb = _quant_pair(x, w, fb.MX32, fb.MX32, layout=fb.SF_TCGEN05)
+    out = _run_mx(qa, sfa, qb, sfb)
+    ref, bound = oracle.gemm(qa, sfa, fb.MX32, qb, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05)
+    bad, worst = within_tolerance(out_f64(out), ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+def test_mx_unit_scales_equal_plain_path():
+    """SF byte 127 (scale 1) everywhere: the block-scaled MMA must equal the plain one."""
+    x, w = synth.tiny()
+    qa, _ = oracle.quantize(x, fb.E4M3, fb.TENSOR)
+    qb, _ = oracle.quantize(w, fb.E4M3, fb.TENSOR)
+    sfa = np.full(oracle.mx_tiled_bytes(128, 512 // 32), 127, np.uint8)
+    sfb = np.full(oracle.mx_tiled_bytes(256, 512 // 32), 127, np.uint8)
+    o_mx = _run_mx(qa, sfa, qb, sfb)
+    one = np.array([1.0], np.float32)
+    o_plain = _run_blockscaled(qa, one, fb.TENSOR, qb, one, fb.TENSOR)
+    assert torch.equal(o_mx, o_plain)
+
+
+def test_mx_distinct_scales_per_row_and_group():
+    """One-hot scale structure: row r of A and group j carry 2^((r + 3j) % 7 - 3)."""
+    M, N, K = 256, 256, 256
+    rng = np.random.default_rng(3)
+    a = oracle.encode(rng.integers(-4, 5, (M, K)).astype(np.float32), fb.E4M3)
+    b = oracle.encode(rng.integers(-4, 5, (N, K)).astype(np.float32), fb.E4M3)
+    ng = K // 32
+    sfa = np.zeros(oracle.mx_tiled_bytes(M, ng), np.uint8)
+    sfb = np.zeros(oracle.mx_tiled_bytes(N, ng), np.uint8)
+    for r in range(M):
+        for j in range(ng):
+            sfa[oracle.mx_tiled_offset(r, j, M, ng)] = 127 + (r + 3 * j) % 7 - 3
+    for n in range(N):
+        for j in range(ng):
+            sfb[oracle.mx_tiled_offset(n, j, N, ng)] = 127 + (2 * n + j) % 5 - 2
+    out = _run_mx(a, sfa, b, sfb)
+    ref, _ = oracle.gemm(a, sfa, fb.MX32, b, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05)
+    expect = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(out_f64(out), expect)
+
+
+# ------------------------------------------------------------------ status
+def test_status_stays_zero_and_launches_counted():
+    x, w = synth.tiny()
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    n0 = fb.launch_count()
+    _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    assert fb.launch_count() == n0 + 1
