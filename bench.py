@@ -1,0 +1,427 @@
+"""Benchmark: FP8 prefill linear layer on one GB300 (or N independent replicas).
+
+One step = the hot path over one batch:
+  quantize X bf16 [4096 x 4096] -> E4M3 with 1x128 tile scales (dynamic)
+  block-scaled GEMM vs W E4M3 [14336 x 4096] with 128x128 block scales
+  (weights quantized once, offline, and resident) -> Out bf16 [4096 x 14336].
+value = 2*M*N*K / step time (TFLOP/s), summed over ranks. L2 is flushed
+(256 MB write) between timed steps; the flush is outside the per-step events.
+
+Besides the headline, the JSON line carries per-kernel measurements of the
+other workloads of the same path (quantizer sweep, decode GEMMs, MXFP8 GEMM),
+each against its roofline, unless --headline-only is given.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the reference arm of this build: there is no other implementation).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% of 4.5 PF); quantize GB/s (% of HBM peak)"
+M, N, K = 4096, 14336, 4096
+WORKLOAD = ("prefill FP8 linear: X bf16 4096x4096 -> E4M3 1x128 tile scales (dynamic), "
+            "W E4M3 14336x4096 128x128 block scales (offline), Out bf16 4096x14336")
+NOMINAL_FP8_PFLOPS = 4.5
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        src = os.path.join(ROOT, "fp8_block_scaled_04_gb300", "csrc", rec["source"])
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        return float(rec["bytes_per_launch"]) if digest == rec["source_sha256"] else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank number over all ranks (identity with one process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time (units per second)."""
+    return world * units_per_rank / (slowest_ms * 1e-3)
+
+
+# --------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from fp8_block_scaled_04_gb300 import binding as fb
+    from fp8_block_scaled_04_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # fp8 = 2 x bf16 (nominal 4.5 / 2.25 PF)
+    hbm_peak = peaks["hbm_gbs"]
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    # ---- inputs (seeded, synthetic); weights quantized once, offline
+    x_host = synth.prefill_x(M, K)
+    w_host = synth.prefill_w(N, K)
+    xd = to_dev(x_host)
+    wd = to_dev(w_host)
+    qw, sw = fb.quantize(wd, fb.E4M3, fb.BLOCK_128x128)
+    del wd
+    qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((K // 128) * M, dtype=torch.float32, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        fb.quantize(xd, fb.E4M3, fb.TILE_1x128, q=qx, scales=sx)
+        fb.gemm_blockscaled(qx, sx, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=out, status=status)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    n0 = fb.launch_count()
+    barrier()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            fb.quantize(xd, fb.E4M3, fb.TILE_1x128, q=qx, scales=sx)
+            e1.record(stream)
+            fb.gemm_blockscaled(qx, sx, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=out, status=status)
+            e2.record(stream)
+        barrier()
+    launches = fb.launch_count() - n0
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    gemm_ms = [b.elapsed_time(c) for _, b, c in ev]
+    quant_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    ms = max_over_ranks(sum(step_ms) / args.steps, dev)
+    assert int(status.item()) == 0, "device status %d" % int(status.item())
+    flops = 2.0 * M * N * K
+    value = whole_job_rate(flops, world, ms) / 1e12
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    achieved = flops / (gemm_avg * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host X in, Out back to pinned host
+    x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_pin = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    xe = torch.empty_like(xd)
+
+    def e2e_step():
+        xe.copy_(x_pin, non_blocking=True)
+        fb.quantize(xe, fb.E4M3, fb.TILE_1x128, q=qx, scales=sx)
+        fb.gemm_blockscaled(qx, sx, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=out, status=status)
+        out_pin.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+
+    extra = {}
+    if not args.headline_only and rank == 0:
+        extra = measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak)
+
+    cpu = cpu_baseline_sample(x_host, w_host) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+            "data": "synthetic: seeded SplitMix64/Box-Muller N(0,1) X with 1% outlier channels x30, N(0,0.02) W",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": "replicas" if world > 1 else "1gpu",
+                       "l2": "flushed between steps (256 MB write, outside the step events)",
+                       "step_ms_quantize": round(sum(quant_ms) / len(quant_ms), 5),
+                       "step_ms_gemm": round(gemm_avg, 5)},
+            "roofline": {"bound": "tensor", "kernel": "gemm_fold_kernel", "achieved": round(achieved, 1),
+                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                         "peak_src": "%s bf16 burst x2 (fp8/bf16 nominal ratio)" % peaks["src"],
+                         "frac_of_nominal_4.5PF": round(achieved / (NOMINAL_FP8_PFLOPS * 1000.0), 4),
+                         "traffic": kernel_traffic("gemm_fold_kernel"),
+                         "algorithmic_bytes": 2 * M * K + N * K + 2 * M * N + 4 * (K // 128) * (M + (N // 128))},
+            "e2e": {"value": round(whole_job_rate(flops, world, e2e) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2, "ms_per_step": round(e2e, 4)},
+            "gpu_launches": int(launches),
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+        }
+        if extra:
+            line["other_workloads"] = extra
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _time_kernel(fn, flush, stream, reps):
+    import torch
+
+    for _ in range(3):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+
+def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak):
+    """Per-kernel numbers for the other workloads of the path, each against its roofline."""
+    import numpy as np
+    import torch
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    res = {}
+    reps = max(10, args.steps)
+    # quantizer sweep: 16384 x 8192, E4M3/E5M2 x {tensor (two-pass), token, 1x128, MX-32}
+    R, C = 16384, 8192
+    x = to_dev(synth.sweep_x(R, C))
+    q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    sweep = {}
+    for fname, fmt in (("e4m3", fb.E4M3), ("e5m2", fb.E5M2)):
+        for gname, gran in (("tensor", fb.TENSOR), ("token", fb.TOKEN), ("tile1x128", fb.TILE_1x128),
+                            ("mx32", fb.MX32)):
+            nb = fb.scales_bytes(R, C, gran)
+            sc = torch.empty(max(nb, 4), dtype=torch.uint8, device=dev)
+            scv = sc if gran == fb.MX32 else sc.view(torch.float32)
+            t = _time_kernel(lambda: fb.quantize(x, fmt, gran, q=q, scales=scv, workspace=ws), flush, stream, reps)
+            byts = R * C * 3 + nb + (R * C * 2 if gran == fb.TENSOR else 0)
+            gbs = byts / (t * 1e-3) / 1e9
+            sweep["%s_%s" % (fname, gname)] = {"ms": round(t, 5), "GB/s": round(gbs, 1),
+                                               "frac_hbm": round(gbs / hbm_peak, 4), "algorithmic_bytes": byts}
+    res["quantize_sweep_16384x8192"] = sweep
+    del x, q
+    # decode-shaped GEMMs: W 18432 x 7168 (132 MB) streamed once
+    Nd, Kd = 18432, 7168
+    wd = to_dev(synth.decode_w(Nd, Kd))
+    qw, sw = fb.quantize(wd, fb.E4M3, fb.BLOCK_128x128)
+    del wd
+    for m in (16, 64):
+        xq, xs = fb.quantize(to_dev(synth.decode_x(m, Kd)), fb.E4M3, fb.TILE_1x128)
+        o = torch.empty((m, Nd), dtype=torch.bfloat16, device=dev)
+        t = _time_kernel(lambda: fb.gemm_blockscaled(xq, xs, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=o),
+                         flush, stream, reps)
+        byts = Nd * Kd + m * Kd + m * Nd * 2 + 4 * (Kd // 128) * (m + Nd // 128)
+        res["decode_gemm_m%d" % m] = {"ms": round(t, 5), "GB/s": round(byts / (t * 1e-3) / 1e9, 1),
+                                      "frac_hbm": round(byts / (t * 1e-3) / 1e9 / hbm_peak, 4),
+                                      "TFLOP/s": round(2.0 * m * Nd * Kd / (t * 1e-3) / 1e12, 2),
+                                      "algorithmic_bytes": byts}
+    del qw, sw
+    # MXFP8 GEMM 8192^3 with UE8M0 per 32 K
+    S = 8192
+    xa, sfa = fb.quantize(to_dev(synth.mx_x(S, S)), fb.E4M3, fb.MX32, fb.SF_TCGEN05)
+    wb, sfb = fb.quantize(to_dev(synth.mx_w(S, S)), fb.E4M3, fb.MX32, fb.SF_TCGEN05)
+    o = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
+    t = _time_kernel(lambda: fb.gemm_mx(xa, sfa, wb, sfb, out=o), flush, stream, reps)
+    tf = 2.0 * S ** 3 / (t * 1e-3) / 1e12
+    res["mx_gemm_8192"] = {"ms": round(t, 5), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
+                           "frac_nominal_4.5PF": round(tf / 4500.0, 4)}
+    return res
+
+
+# --------------------------------------------------------------------- CPU oracle
+def cpu_baseline_sample(x_host, w_host, target_s: float = 10.0):
+    """The oracle as it stands, on a bounded sample of the headline workload:
+    quantize the first R rows of X (1x128), quantize W (128x128), and the fp64
+    GEMM of those R rows against all of W. Scaled to TFLOP/s of that sample."""
+    import oracle
+
+    threads = oracle.default_threads()
+    qb, sb = oracle.quantize(w_host, oracle.E4M3, oracle.BLOCK_128x128)
+    rows = 8
+    while True:
+        t0 = time.perf_counter()
+        qa, sa = oracle.quantize(x_host[:rows], oracle.E4M3, oracle.TILE_1x128)
+        oracle.gemm(qa, sa, oracle.TILE_1x128, qb, sb, oracle.BLOCK_128x128)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or rows >= M:
+            break
+        rows = min(M, max(rows * 2, int(rows * target_s / max(dt, 1e-3))))
+    flops = 2.0 * rows * N * K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "first %d of %d rows of X, all of W (%dx%d), fp64 sums; %.1f s" % (rows, M, N, K, dt)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from fp8_block_scaled_04_gb300 import synth
+    import oracle
+
+    x_host = synth.prefill_x(M, K)
+    w_host = synth.prefill_w(N, K)
+    threads = oracle.default_threads()
+    qb, sb = oracle.quantize(w_host, oracle.E4M3, oracle.BLOCK_128x128)
+    rows = 4
+
+    def one_step():
+        qa, sa = oracle.quantize(x_host[:rows], oracle.E4M3, oracle.TILE_1x128)
+        oracle.gemm(qa, sa, oracle.TILE_1x128, qb, sb, oracle.BLOCK_128x128)
+
+    # size the per-step sample so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    one_step()
+    dt = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(M, rows * budget / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    sec = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * N * K / sec / 1e12
+    sample = "first %d of %d rows of X per step, all of W (%dx%d), fp64 sums" % (rows, M, N, K)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
