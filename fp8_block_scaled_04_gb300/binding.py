@@ -44,6 +44,8 @@ def lib():
         L.fp8_quantize_workspace_bytes.argtypes = [i64, i64, i32]
         L.fp8_quantize.restype = i32
         L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, sz, vp]
+        L.fp8_quantize_tensor_noalloc.restype = i32
+        L.fp8_quantize_tensor_noalloc.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, vp]
         L.fp8_dequantize.restype = i32
         L.fp8_dequantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp]
         L.fp8_gemm_blockscaled.restype = i32

@@ -150,6 +150,24 @@ fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+fp8_status_t fp8_quantize_tensor_noalloc(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x,
+                                         fp8_format_t fmt, void *q_dev, int64_t ld_q, float *scale_dev,
+                                         fp8_stream_t stream) {
+  if (!valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  fp8_status_t st = check_quant_shape(rows, cols, FP8_GRAN_TENSOR);
+  if (st != FP8_OK) return st;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (x_dev == nullptr || q_dev == nullptr || scale_dev == nullptr) return FP8_ERR_INVALID_ARG;
+  if (ld_x < cols || ld_q < cols) return FP8_ERR_INVALID_ARG;
+  if (!aligned(x_dev, 16) || !aligned(q_dev, 16) || ld_x % 8 || ld_q % 16) return FP8_ERR_ALIGNMENT;
+  if (!aligned(scale_dev, 4)) return FP8_ERR_ALIGNMENT;
+  const size_t need = fp8_quantize_workspace_bytes(rows, cols, FP8_GRAN_TENSOR);
+  if (need > noalloc_scratch_capacity()) return FP8_ERR_WORKSPACE;
+  return launch_quantize_tensor_noalloc(static_cast<const uint16_t *>(x_dev), rows, cols, ld_x, fmt,
+                                        static_cast<uint8_t *>(q_dev), ld_q, scale_dev, need,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
 fp8_status_t fp8_dequantize(const void *q_dev, int64_t rows, int64_t cols, int64_t ld_q, fp8_format_t fmt,
                             fp8_gran_t gran, fp8_sf_layout_t sf_layout, const void *scales_dev, void *out_dev,
                             int64_t ld_out, fp8_stream_t stream) {

@@ -23,6 +23,14 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
                              int sf_layout, const float *static_scale, uint8_t *q, int64_t ld_q, void *scales,
                              void *workspace, cudaStream_t stream);
 
+// Per-tensor quantization with its amax scratch in a static device array
+// (no workspace argument, no allocation). Refuses scratch_needed beyond the
+// array's capacity with FP8_ERR_WORKSPACE.
+fp8_status_t launch_quantize_tensor_noalloc(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                            uint8_t *q, int64_t ld_q, float *scale_out, size_t scratch_needed,
+                                            cudaStream_t stream);
+size_t noalloc_scratch_capacity();
+
 fp8_status_t launch_encode_f32(const float *x, int64_t n, int fmt, uint8_t *out, cudaStream_t stream);
 
 fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, int fmt, int gran,

@@ -20,6 +20,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -543,6 +545,75 @@ fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int
   else
     dequant_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
   note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace fp8bs
+
+// ---------------------------------------------------------------------------
+// Allocation-free per-tensor quantization.
+//
+// Some callers cannot call cudaMalloc: code running inside a host framework
+// that owns every byte of device memory (a fixed arena handed to plugins with
+// no allocator behind it), or a latency-critical path on which cudaMalloc's
+// implicit device-wide synchronisation is not acceptable. For them the grid-wide
+// amax of the two-pass per-tensor quantizer lives in this file-scope device
+// array instead of a caller-provided workspace. Every GPU that loads the
+// library holds these bytes until the process exits.
+//
+// In host code the name g_noalloc_scratch is only a host-side stand-in for the
+// symbol, not a device address; the device address comes from
+// cudaGetSymbolAddress, taken once per device (with that device current) on the
+// first call made on that device. All calls share the array: each call clears
+// the amax word before using it, and calls whose kernels overlap on the GPU
+// (different streams, no ordering between them) race on it.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace fp8bs {
+namespace {
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxScratchDevices] = {};
+}  // namespace
+
+size_t noalloc_scratch_capacity() { return kNoAllocScratchBytes; }
+
+// Device address of g_noalloc_scratch on the current device (set up once per device).
+static fp8_status_t noalloc_scratch_address(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return FP8_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return FP8_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return FP8_OK;
+}
+
+fp8_status_t launch_quantize_tensor_noalloc(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                            uint8_t *q, int64_t ld_q, float *scale_out, size_t scratch_needed,
+                                            cudaStream_t stream) {
+  if (scratch_needed > kNoAllocScratchBytes) return FP8_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const fp8_status_t st = noalloc_scratch_address(&scratch);
+  if (st != FP8_OK) return st;
+  uint32_t *amax = static_cast<uint32_t *>(scratch);
+  if (cudaMemsetAsync(amax, 0, sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
+  const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
+  const int grid = stream_grid(tasks);
+  amax_kernel<<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, amax);
+  if (fmt == FP8_E4M3)
+    quant_tensor_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scale_out, amax,
+                                                                 nullptr);
+  else
+    quant_tensor_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scale_out, amax,
+                                                                 nullptr);
+  note_launches(2);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -122,6 +122,30 @@ fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t
                           int64_t ld_q, void *scales_dev, void *workspace_dev, size_t workspace_bytes,
                           fp8_stream_t stream);
 
+/* Dynamic per-tensor quantization that allocates nothing and takes no
+ * workspace. The pages have no counterpart to this entry point; it exists for
+ * callers that cannot call cudaMalloc -- code inside a host framework that owns
+ * all device memory (a fixed arena with no allocator exposed to plugins), or a
+ * latency-critical path where cudaMalloc's implicit device synchronisation is
+ * not acceptable.
+ * Computes exactly what fp8_quantize computes for FP8_GRAN_TENSOR without a
+ * static scale (same kernels, same results): q_dev [rows x cols] (ld_q bytes)
+ * and the single fp32 scale in *scale_dev.
+ * Scratch: the grid-wide amax lives in a 256-byte static device array inside
+ * the library (every GPU that loads the library holds it until the process
+ * exits). A call whose scratch need (fp8_quantize_workspace_bytes for
+ * FP8_GRAN_TENSOR) exceeds those 256 bytes is refused with FP8_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call clears the amax word before it starts, but all calls
+ * share the array: calls whose kernels overlap on the GPU (unordered streams)
+ * race and must be serialised by the caller.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ * Shape and alignment rules as fp8_quantize with FP8_GRAN_TENSOR. */
+fp8_status_t fp8_quantize_tensor_noalloc(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x,
+                                         fp8_format_t fmt, void *q_dev, int64_t ld_q, float *scale_dev,
+                                         fp8_stream_t stream);
+
 /* Dequantization ("07 -- The FP8 Family": x_hat = x_fp8 * s; "Low precision",
  * qdq_e4m3 listing: exact decode, then one fp32 multiply by s):
  * out = bf16_RN(fp32(decode(q) * s)). Same layouts and rules as fp8_quantize;
