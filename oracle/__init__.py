@@ -18,7 +18,7 @@ import numpy as np
 from . import build as _build
 
 E4M3, E5M2 = 0, 1
-TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32 = 0, 1, 2, 3, 4
+TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32, CHANNEL = 0, 1, 2, 3, 4, 5
 SF_LINEAR, SF_TILED = 0, 1
 
 _lib = None
@@ -65,6 +65,8 @@ def lib():
         L.orc_gemm.restype = c_int
         L.orc_gemm.argtypes = [vp, c_i64, vp, c_int, c_int, c_int, vp, c_i64, vp, c_int, c_int, c_int,
                                c_i64, c_i64, c_i64, vp, c_i64, vp, c_i64, vp, vp, c_int]
+        L.orc_quantize_delayed.restype = c_int
+        L.orc_quantize_delayed.argtypes = [vp, c_i64, c_i64, c_int, vp, c_int, c_int, c_int, vp, vp, vp, c_int]
         L.orc_default_threads.restype = c_int
         L.orc_default_threads.argtypes = []
         _lib = L
@@ -158,6 +160,8 @@ def scales_shape(rows: int, cols: int, gran: int, sf_layout: int = SF_LINEAR):
         return np.float32, (cols // 128) * rows
     if gran == BLOCK_128x128:
         return np.float32, ((rows + 127) // 128) * (cols // 128)
+    if gran == CHANNEL:
+        return np.float32, cols
     if gran == MX32:
         if sf_layout == SF_TILED:
             return np.uint8, mx_tiled_bytes(rows, cols // 32)
@@ -179,6 +183,24 @@ def quantize(x_bf16: np.ndarray, fmt: int, gran: int, sf_layout: int = SF_LINEAR
     if rc != 0:
         raise ValueError("oracle quantize rejected the arguments (rc=%d)" % rc)
     return q, sc[:n]
+
+
+def quantize_delayed(x_bf16: np.ndarray, fmt: int, history, slot: int, margin: int = 0, nthreads: int = 0):
+    """Per-tensor quantization with the scale taken from an amax history.
+
+    Returns (q, scale, new_history) where new_history[slot] = amax(x).
+    """
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, cols = x.shape
+    h = np.ascontiguousarray(history, dtype=np.float32)
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.zeros(1, dtype=np.float32)
+    nh = np.empty_like(h)
+    rc = lib().orc_quantize_delayed(_p(x), rows, cols, fmt, _p(h), h.size, slot, margin, _p(q), _p(s), _p(nh),
+                                    nthreads)
+    if rc != 0:
+        raise ValueError("oracle quantize_delayed rejected the arguments (rc=%d)" % rc)
+    return q, s, nh
 
 
 def dequantize(q: np.ndarray, scales: np.ndarray, fmt: int, gran: int, sf_layout: int = SF_LINEAR,

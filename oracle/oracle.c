@@ -31,6 +31,7 @@
 #define ORC_GRAN_TILE_1x128 2
 #define ORC_GRAN_BLOCK_128x128 3
 #define ORC_GRAN_MX32 4
+#define ORC_GRAN_CHANNEL 5
 
 #define ORC_SF_LINEAR 0
 #define ORC_SF_TILED 1
@@ -459,6 +460,21 @@ static void q_blocks(void *p, int64_t lo, int64_t hi, int tid) {
   }
 }
 
+/* per-channel (one scale per column): "FP8 Serving" guide, Things to try
+   (per-channel scales for the KV cache, whose outliers are channel-structured);
+   "FP8 Mixed-Precision Serving", FP8 KV Cache section. */
+static void q_channel_cols(void *p, int64_t lo, int64_t hi, int tid) {
+  (void)tid;
+  qctx *c = (qctx *)p;
+  float *sf = (float *)c->scales;
+  for (int64_t k = lo; k < hi; ++k) {
+    float s, si;
+    scale_from_amax(group_amax(c, 0, c->rows, k, k + 1), c->fmt, &s, &si);
+    sf[k] = s;
+    group_encode(c, 0, c->rows, k, k + 1, si);
+  }
+}
+
 static void amax_rows(void *p, int64_t lo, int64_t hi, int tid) {
   qctx *c = (qctx *)p;
   c->tensor_amax_part[tid] = group_amax(c, lo, hi, 0, c->cols);
@@ -471,6 +487,7 @@ int orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int
   if ((gran == ORC_GRAN_TILE_1x128 || gran == ORC_GRAN_BLOCK_128x128) && cols % 128) return -1;
   if (gran == ORC_GRAN_MX32 && cols % 32) return -1;
   if (static_scale && gran != ORC_GRAN_TENSOR) return -1;
+  if (gran == ORC_GRAN_CHANNEL && cols % 16) return -1;
   qctx c;
   memset(&c, 0, sizeof c);
   c.x = x;
@@ -518,9 +535,64 @@ int orc_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int
     case ORC_GRAN_BLOCK_128x128:
       parallel_for((rows + 127) / 128, nthreads, q_blocks, &c);
       return 0;
+    case ORC_GRAN_CHANNEL:
+      parallel_for(cols, nthreads, q_channel_cols, &c);
+      return 0;
     default:
       return -1;
   }
+}
+
+/* Delayed scaling ("FP8 Mixed-Precision Serving", Delayed Scaling vs.
+   Just-in-Time Dynamic Scaling: rho = FP8Max / (2^m * max(H)) over an amax
+   history H; "Low precision", NVIDIA's taxonomy: per-tensor, delayed).
+   Reading: the multiplier rho is formed the way the other scales are:
+   s = fp32(fp32(2^m * max(H)) / V_max), rho = s_inv = fp32(1 / s) (0 rule as
+   above); an empty or non-finite history (max(H) == 0, inf or NaN) uses s = 1.
+   The tensor's own amax then replaces history[slot] (the oldest entry of a
+   ring the caller advances one slot per step). */
+int orc_quantize_delayed(const uint16_t *x, int64_t rows, int64_t cols, int fmt, const float *history, int hlen,
+                         int slot, int margin, uint8_t *q, float *scale_out, float *new_history, int nthreads) {
+  if (rows < 0 || cols < 0 || hlen <= 0 || slot < 0 || slot >= hlen || (fmt != ORC_E4M3 && fmt != ORC_E5M2))
+    return -1;
+  float mh = 0.0f;
+  int bad = 0;
+  for (int i = 0; i < hlen; ++i) {
+    if (!isfinite(history[i])) bad = 1;
+    if (history[i] > mh) mh = history[i];
+  }
+  float s, si;
+  if (bad || mh == 0.0f) {
+    s = 1.0f;
+    si = 1.0f;
+  } else {
+    float scaled = ldexpf(mh, margin);
+    s = scaled / vmax_f(fmt);
+    si = 1.0f / s;
+    if (s == 0.0f || !isfinite(si)) si = 0.0f;
+  }
+  qctx c;
+  memset(&c, 0, sizeof c);
+  c.x = x;
+  c.rows = rows;
+  c.cols = cols;
+  c.ldx = cols;
+  c.fmt = fmt;
+  c.gran = ORC_GRAN_TENSOR;
+  c.q = q;
+  c.ldq = cols;
+  c.tensor_s = s;
+  c.tensor_s_inv = si;
+  int nt = resolve_threads(nthreads);
+  parallel_for(rows, nt, amax_rows, &c);
+  float amax = 0.0f;
+  for (int t = 0; t < 256; ++t)
+    if (c.tensor_amax_part[t] > amax || isnan(c.tensor_amax_part[t])) amax = c.tensor_amax_part[t];
+  parallel_for(rows, nthreads, q_rows, &c);
+  *scale_out = s;
+  for (int i = 0; i < hlen; ++i) new_history[i] = history[i];
+  new_history[slot] = amax;
+  return 0;
 }
 
 /* ------------------------------------------------------------------ */
@@ -539,6 +611,8 @@ static double elem_scale(const void *scales, int gran, int sf_layout, int64_t r,
       return sf[(k / 128) * rows + r];
     case ORC_GRAN_BLOCK_128x128:
       return sf[(r / 128) * (cols / 128) + k / 128];
+    case ORC_GRAN_CHANNEL:
+      return sf[k];
     case ORC_GRAN_MX32: {
       int64_t ng = cols / 32;
       uint8_t b = sf_layout == ORC_SF_TILED ? sb[orc_mx_tiled_offset(r, k / 32, rows, ng)] : sb[r * ng + k / 32];

@@ -266,3 +266,92 @@ def test_underflow_probe_from_guide():
                 assert rel == pytest.approx(100.0)
             else:
                 assert 1.5 <= rel <= 3.0, (mag, tag, rel)  # the page prints ~2.1-2.2%
+
+
+# ------------------------------------------------------------ per-channel
+def test_channel_is_token_of_transpose():
+    """Per-channel scaling of X is per-token scaling of X^T (one scale per column)."""
+    from oracle import CHANNEL
+
+    x = synth.bf16_matrix(96, 272, 1.0, 71, 72, 0.02, 50.0)
+    q, s = oracle.quantize(x, E4M3, CHANNEL)
+    qt, st = oracle.quantize(np.ascontiguousarray(x.T), E4M3, TOKEN)
+    assert np.array_equal(q, qt.T)
+    assert np.array_equal(f32(s), f32(st))
+
+
+def f32(a):
+    return np.asarray(a, dtype=np.float32).view(np.uint32)
+
+
+def test_channel_amax_hits_vmax_per_column():
+    from oracle import CHANNEL
+
+    x = synth.bf16_matrix(130, 64, 1.0, 73, 74, 0.05, 80.0)
+    for fmt in (E4M3, E5M2):
+        q, s = oracle.quantize(x, fmt, CHANNEL)
+        xf = np.abs(_f32(x))
+        for k in range(64):
+            col = xf[:, k]
+            assert np.all((q[:, k][col == col.max()] & 0x7F) == MAXC[fmt])
+            assert np.float32(col.max()) / np.float32(VMAX[fmt]) == s[k]
+
+
+def test_channel_dequantize_roundtrip():
+    from oracle import CHANNEL
+
+    x = synth.bf16_matrix(40, 128, 1.0, 75)
+    q, s = oracle.quantize(x, E4M3, CHANNEL)
+    xh = _f32(oracle.dequantize(q, s, E4M3, CHANNEL)).astype(np.float64)
+    xf = _f32(x).astype(np.float64)
+    sc = np.repeat(s.astype(np.float64)[None, :], 40, axis=0)
+    assert np.all(np.abs(xh - xf) <= 2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * sc + 2.0 ** -8 * np.abs(xh) + 1e-45)
+
+
+# ------------------------------------------------------------ delayed scaling
+def test_delayed_with_own_amax_equals_current_scaling():
+    x = synth.bf16_matrix(64, 512, 1.0, 81, 82, 0.01, 20.0)
+    amax = float(np.abs(_f32(x)).max())
+    for fmt in (E4M3, E5M2):
+        qd, sd, nh = oracle.quantize_delayed(x, fmt, [amax, 0.0, 0.0], slot=1)
+        qc, sc = oracle.quantize(x, fmt, TENSOR)
+        assert np.array_equal(qd, qc) and sd[0] == sc[0]
+        assert nh[1] == np.float32(amax) and nh[0] == np.float32(amax) and nh[2] == 0.0
+
+
+def test_delayed_margin_is_power_of_two_on_scale():
+    x = synth.bf16_matrix(32, 256, 1.0, 83)
+    hist = np.array([3.5, 1.25, 7.0, 2.0], np.float32)
+    q0, s0, _ = oracle.quantize_delayed(x, E4M3, hist, slot=0, margin=0)
+    q2, s2, _ = oracle.quantize_delayed(x, E4M3, hist, slot=0, margin=2)
+    assert s0[0] == np.float32(7.0) / np.float32(448.0)
+    assert s2[0] == s0[0] * 4
+    # the codes are those of static scaling with that scale
+    qs, _ = oracle.quantize(x, E4M3, TENSOR, static_scale=float(s2[0]))
+    assert np.array_equal(q2, qs)
+
+
+def test_delayed_history_ring_and_saturation():
+    hist = np.zeros(4, np.float32)
+    xs = [synth.bf16_matrix(16, 128, sig, 90 + i) for i, sig in enumerate([1.0, 1.0, 8.0, 0.5])]
+    for step, x in enumerate(xs):
+        q, s, hist2 = oracle.quantize_delayed(x, E4M3, hist, slot=step % 4)
+        amax = float(np.abs(_f32(x)).max())
+        assert hist2[step % 4] == np.float32(amax)
+        if step == 0:
+            assert s[0] == 1.0  # empty history: identity scale
+        if step == 2:
+            # the history only knew the sigma-1 tensors: the sigma-8 outliers saturate at +-448
+            dec = np.abs(oracle.decode(q, E4M3))
+            assert np.any(dec == 448.0) and np.abs(_f32(x)).max() * (1 / s[0]) > 448.0
+        hist = hist2
+    assert np.array_equal(hist[:4] > 0, [True, True, True, True])
+
+
+def test_delayed_nonfinite_history_uses_unit_scale():
+    x = synth.bf16_matrix(8, 128, 1.0, 95)
+    for bad in (np.inf, np.nan):
+        q, s, _ = oracle.quantize_delayed(x, E4M3, [1.0, bad], slot=0)
+        assert s[0] == 1.0
+        qs, _ = oracle.quantize(x, E4M3, TENSOR, static_scale=1.0)
+        assert np.array_equal(q, qs)
