@@ -205,30 +205,54 @@ def run_gpu(args):
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     achieved = flops / (gemm_avg * 1e-3) / 1e12
 
-    # ---- end to end through the public API: pinned host X in, Out back to pinned host
+    # ---- end to end through the public API: pinned host X in, Out back to pinned host.
+    # Every step copies its X host->device and its Out device->host; steps are
+    # pipelined over three streams (copy-in, compute, copy-out) with two device
+    # buffers each, so step i+1's upload and step i-1's download overlap step i's
+    # kernels. The timed region runs from the first upload to the last download.
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_pin = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    xe = torch.empty_like(xd)
+    out_pin = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xe = [torch.empty_like(xd) for _ in range(2)]
+    oe = [torch.empty_like(out) for _ in range(2)]
+    qxe = [torch.empty_like(qx) for _ in range(2)]
+    sxe = [torch.empty_like(sx) for _ in range(2)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        xe.copy_(x_pin, non_blocking=True)
-        fb.quantize(xe, fb.E4M3, fb.TILE_1x128, q=qx, scales=sx)
-        fb.gemm_blockscaled(qx, sx, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=out, status=status)
-        out_pin.copy_(out, non_blocking=True)
+    def e2e_run(nsteps):
+        ev_x_ready = [torch.cuda.Event() for _ in range(2)]
+        ev_x_free = [torch.cuda.Event() for _ in range(2)]
+        ev_o_ready = [torch.cuda.Event() for _ in range(2)]
+        ev_o_free = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(nsteps):
+            b = i & 1
+            if i >= 2:
+                s_in.wait_event(ev_x_free[b])
+            with torch.cuda.stream(s_in):
+                xe[b].copy_(x_pin, non_blocking=True)
+            ev_x_ready[b].record(s_in)
+            s_cmp.wait_event(ev_x_ready[b])
+            if i >= 2:
+                s_cmp.wait_event(ev_o_free[b])
+            fb.quantize(xe[b], fb.E4M3, fb.TILE_1x128, q=qxe[b], scales=sxe[b], stream=s_cmp)
+            fb.gemm_blockscaled(qxe[b], sxe[b], fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=oe[b], status=status,
+                                stream=s_cmp)
+            ev_x_free[b].record(s_cmp)
+            ev_o_ready[b].record(s_cmp)
+            s_out.wait_event(ev_o_ready[b])
+            with torch.cuda.stream(s_out):
+                out_pin[b].copy_(oe[b], non_blocking=True)
+            ev_o_free[b].record(s_out)
+        s_in.wait_stream(s_out)
+        t1.record(s_in)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / nsteps
 
-    for _ in range(args.warmup):
-        e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+    e2e_run(args.warmup)
+    torch.cuda.synchronize()
+    e2e = max_over_ranks(e2e_run(args.steps), dev)
 
     extra = {}
     if not args.headline_only and rank == 0:
@@ -253,7 +277,8 @@ def run_gpu(args):
                          "traffic": kernel_traffic("gemm_fold_kernel"),
                          "algorithmic_bytes": 2 * M * K + N * K + 2 * M * N + 4 * (K // 128) * (M + (N // 128))},
             "e2e": {"value": round(whole_job_rate(flops, world, e2e) / 1e12, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2, "ms_per_step": round(e2e, 4)},
+                    "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2, "ms_per_step": round(e2e, 4),
+                    "pipelining": "3 streams (upload / compute / download), 2 buffers each, across steps"},
             "gpu_launches": int(launches),
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -284,17 +309,15 @@ def _time_kernel(fn, flush, stream, reps):
     return statistics.median(a.elapsed_time(b) for a, b in ts)
 
 
-def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak):
-    """Per-kernel numbers for the other workloads of the path, each against its roofline."""
+def measure_sweep(args, fb, synth, dev, stream, flush, hbm_peak):
+    """Quantizer sweep: 16384 x 8192, E4M3/E5M2 x {tensor (two-pass), token, 1x128, MX-32}."""
     import numpy as np
     import torch
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    res = {}
     reps = max(10, args.steps)
-    # quantizer sweep: 16384 x 8192, E4M3/E5M2 x {tensor (two-pass), token, 1x128, MX-32}
     R, C = 16384, 8192
     x = to_dev(synth.sweep_x(R, C))
     q = torch.empty((R, C), dtype=torch.uint8, device=dev)
@@ -311,9 +334,19 @@ def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_p
             gbs = byts / (t * 1e-3) / 1e9
             sweep["%s_%s" % (fname, gname)] = {"ms": round(t, 5), "GB/s": round(gbs, 1),
                                                "frac_hbm": round(gbs / hbm_peak, 4), "algorithmic_bytes": byts}
-    res["quantize_sweep_16384x8192"] = sweep
-    del x, q
-    # decode-shaped GEMMs: W 18432 x 7168 (132 MB) streamed once
+    return sweep
+
+
+def measure_decode(args, fb, synth, dev, stream, flush, hbm_peak):
+    """Decode-shaped GEMMs: W 18432 x 7168 (132 MB) streamed once per call, M = 16 and 64."""
+    import numpy as np
+    import torch
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    reps = max(10, args.steps)
+    res = {}
     Nd, Kd = 18432, 7168
     wd = to_dev(synth.decode_w(Nd, Kd))
     qw, sw = fb.quantize(wd, fb.E4M3, fb.BLOCK_128x128)
@@ -328,16 +361,55 @@ def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_p
                                       "frac_hbm": round(byts / (t * 1e-3) / 1e9 / hbm_peak, 4),
                                       "TFLOP/s": round(2.0 * m * Nd * Kd / (t * 1e-3) / 1e12, 2),
                                       "algorithmic_bytes": byts}
-    del qw, sw
-    # MXFP8 GEMM 8192^3 with UE8M0 per 32 K
+    return res
+
+
+def measure_mx(args, fb, synth, dev, stream, flush, fp8_peak):
+    """MXFP8 GEMM 8192^3 with UE8M0 scales per 32 K (tensor-core block scaling)."""
+    import numpy as np
+    import torch
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    reps = max(10, args.steps)
     S = 8192
     xa, sfa = fb.quantize(to_dev(synth.mx_x(S, S)), fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     wb, sfb = fb.quantize(to_dev(synth.mx_w(S, S)), fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     o = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
     t = _time_kernel(lambda: fb.gemm_mx(xa, sfa, wb, sfb, out=o), flush, stream, reps)
     tf = 2.0 * S ** 3 / (t * 1e-3) / 1e12
-    res["mx_gemm_8192"] = {"ms": round(t, 5), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
-                           "frac_nominal_4.5PF": round(tf / 4500.0, 4)}
+    return {"mx_gemm_8192": {"ms": round(t, 5), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
+                             "frac_nominal_4.5PF": round(tf / 4500.0, 4)}}
+
+
+def run_workload(args):
+    """One non-headline workload on its own (for profiling): prints one JSON line."""
+    import torch
+
+    from fp8_block_scaled_04_gb300 import binding as fb
+    from fp8_block_scaled_04_gb300 import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = flush_buf.zero_
+    if args.workload == "sweep":
+        res = {"quantize_sweep_16384x8192": measure_sweep(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"])}
+    elif args.workload == "decode":
+        res = measure_decode(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"])
+    else:
+        res = measure_mx(args, fb, synth, dev, stream, flush, 2.0 * peaks["bf16_tflops"])
+    print(json.dumps({"workload": args.workload, "peaks": peaks["src"], "results": res}))
+
+
+def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak):
+    """Per-kernel numbers for the other workloads of the path, each against its roofline."""
+    res = {"quantize_sweep_16384x8192": measure_sweep(args, fb, synth, dev, stream, flush, hbm_peak)}
+    res.update(measure_decode(args, fb, synth, dev, stream, flush, hbm_peak))
+    res.update(measure_mx(args, fb, synth, dev, stream, flush, fp8_peak))
     return res
 
 
@@ -413,12 +485,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--workload", default="all", choices=["all", "sweep", "decode", "mx"],
+                    help="all: the headline step plus the other workloads; otherwise that workload alone")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "all":
+        run_workload(args)
     else:
         run_gpu(args)
 

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "libfp8bs.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "fp8bs.h")
 
 E4M3, E5M2 = 0, 1
-TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32 = 0, 1, 2, 3, 4
+TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32, CHANNEL = 0, 1, 2, 3, 4, 5
 SF_LINEAR, SF_TCGEN05 = 0, 1
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
@@ -46,10 +46,14 @@ def lib():
         L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, sz, vp]
         L.fp8_quantize_tensor_noalloc.restype = i32
         L.fp8_quantize_tensor_noalloc.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, vp]
+        L.fp8_quantize_delayed.restype = i32
+        L.fp8_quantize_delayed.argtypes = [vp, i64, i64, i64, i32, vp, i32, i32, i32, vp, i64, vp, vp]
         L.fp8_dequantize.restype = i32
         L.fp8_dequantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp]
         L.fp8_gemm_blockscaled.restype = i32
         L.fp8_gemm_blockscaled.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp, vp]
+        L.fp8_gemm_blockscaled_quantized_out.restype = i32
+        L.fp8_gemm_blockscaled_quantized_out.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp]
         L.fp8_gemm_mx.restype = i32
         L.fp8_gemm_mx.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
         L.fp8_debug_encode_f32.restype = i32
@@ -123,13 +127,30 @@ def quantize(x, fmt: int, gran: int, sf_layout: int = SF_LINEAR, static_scale=No
         else:
             scales = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)[: nbytes // 4]
     wsb = workspace_bytes(rows, cols, gran)
-    if workspace is None and wsb > 0 and static_scale is None:
+    if workspace is None and wsb > 0 and (static_scale is None or gran == CHANNEL):
         workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     rc = lib().fp8_quantize(_ptr(x), rows, cols, x.stride(0), fmt, gran, sf_layout, _ptr(static_scale), _ptr(q),
                             q.stride(0), _ptr(scales), _ptr(workspace),
                             0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "fp8_quantize")
     return q, scales
+
+
+def quantize_delayed(x, fmt: int, history, slot: int, margin: int = 0, q=None, scale=None, stream=None):
+    """Per-tensor quantization with the scale from an amax history (updated in place at `slot`)."""
+    import torch
+
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert history.dtype == torch.float32 and history.is_contiguous()
+    rows, cols = x.shape
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    rc = lib().fp8_quantize_delayed(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(history), history.numel(), slot,
+                                    margin, _ptr(q), q.stride(0), _ptr(scale), _stream(stream))
+    _check(rc, "fp8_quantize_delayed")
+    return q, scale
 
 
 def dequantize(q, scales, fmt: int, gran: int, sf_layout: int = SF_LINEAR, out=None, stream=None):
@@ -160,6 +181,28 @@ def gemm_blockscaled(a, a_scales, a_gran: int, b, b_scales, b_gran: int, a_fmt: 
                                     _ptr(out), M, N, K, _ptr(status), _stream(stream))
     _check(rc, "fp8_gemm_blockscaled")
     return out
+
+
+def gemm_blockscaled_quantized_out(a, a_scales, b, b_scales, a_fmt: int = E4M3, b_fmt: int = E4M3,
+                                   out_fmt: int = E4M3, q_out=None, q_scales=None, status=None, stream=None):
+    """Block-scaled GEMM whose epilogue quantizes the bf16 output at 1x128.
+
+    Returns (q uint8 [M, N], scales float32 [(N/128) * M]) in the 1x128 tile layout.
+    """
+    import torch
+
+    M, K = a.shape
+    N, K2 = b.shape
+    assert K == K2 and a.is_contiguous() and b.is_contiguous()
+    if q_out is None:
+        q_out = torch.empty((M, N), dtype=torch.uint8, device=a.device)
+    if q_scales is None:
+        q_scales = torch.empty((N // 128) * M, dtype=torch.float32, device=a.device)
+    rc = lib().fp8_gemm_blockscaled_quantized_out(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), a_fmt, b_fmt,
+                                                  out_fmt, _ptr(q_out), _ptr(q_scales), M, N, K, _ptr(status),
+                                                  _stream(stream))
+    _check(rc, "fp8_gemm_blockscaled_quantized_out")
+    return q_out, q_scales
 
 
 def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, status=None, stream=None):

@@ -25,7 +25,7 @@ std::once_flag g_encode_once;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
-bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_MX32; }
+bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_CHANNEL; }
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 }  // namespace
 
@@ -93,6 +93,7 @@ size_t fp8_scales_bytes(int64_t rows, int64_t cols, fp8_gran_t gran, fp8_sf_layo
   switch (gran) {
     case FP8_GRAN_TENSOR: return sizeof(float);
     case FP8_GRAN_TOKEN: return static_cast<size_t>(rows) * sizeof(float);
+    case FP8_GRAN_CHANNEL: return static_cast<size_t>(cols) * sizeof(float);
     case FP8_GRAN_TILE_1x128:
       return cols % 128 ? 0 : static_cast<size_t>(cols / 128) * static_cast<size_t>(rows) * sizeof(float);
     case FP8_GRAN_BLOCK_128x128:
@@ -109,15 +110,17 @@ size_t fp8_scales_bytes(int64_t rows, int64_t cols, fp8_gran_t gran, fp8_sf_layo
 
 size_t fp8_quantize_workspace_bytes(int64_t rows, int64_t cols, fp8_gran_t gran) {
   (void)rows;
-  (void)cols;
-  return gran == FP8_GRAN_TENSOR ? 256 : 0;
+  if (gran == FP8_GRAN_TENSOR) return 256;
+  if (gran == FP8_GRAN_CHANNEL && cols > 0) return (static_cast<size_t>(cols) * sizeof(float) + 255) / 256 * 256;
+  return 0;
 }
 
 static fp8_status_t check_quant_shape(int64_t rows, int64_t cols, int gran) {
   if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return FP8_ERR_UNSUPPORTED_SHAPE;
   switch (gran) {
     case FP8_GRAN_TENSOR:
-    case FP8_GRAN_TOKEN: return cols % 16 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
+    case FP8_GRAN_TOKEN:
+    case FP8_GRAN_CHANNEL: return cols % 16 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
     case FP8_GRAN_TILE_1x128:
     case FP8_GRAN_BLOCK_128x128: return cols % 128 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
     case FP8_GRAN_MX32: return cols % 32 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
@@ -140,7 +143,7 @@ fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t
   if (ld_x < cols || ld_q < cols) return FP8_ERR_INVALID_ARG;
   if (!aligned(x_dev, 16) || !aligned(q_dev, 16) || ld_x % 8 || ld_q % 16) return FP8_ERR_ALIGNMENT;
   if (!aligned(scales_dev, 4) || (static_scale_dev && !aligned(static_scale_dev, 4))) return FP8_ERR_ALIGNMENT;
-  if (gran == FP8_GRAN_TENSOR && static_scale_dev == nullptr) {
+  if ((gran == FP8_GRAN_TENSOR && static_scale_dev == nullptr) || gran == FP8_GRAN_CHANNEL) {
     if (workspace_dev == nullptr || workspace_bytes < fp8_quantize_workspace_bytes(rows, cols, gran))
       return FP8_ERR_WORKSPACE;
     if (!aligned(workspace_dev, 4)) return FP8_ERR_ALIGNMENT;
@@ -166,6 +169,24 @@ fp8_status_t fp8_quantize_tensor_noalloc(const void *x_dev, int64_t rows, int64_
   return launch_quantize_tensor_noalloc(static_cast<const uint16_t *>(x_dev), rows, cols, ld_x, fmt,
                                         static_cast<uint8_t *>(q_dev), ld_q, scale_dev, need,
                                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_quantize_delayed(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x, fp8_format_t fmt,
+                                  float *amax_history_dev, int32_t history_len, int32_t slot, int32_t margin,
+                                  void *q_dev, int64_t ld_q, float *scale_dev, fp8_stream_t stream) {
+  if (!valid_fmt(fmt)) return FP8_ERR_INVALID_ARG;
+  if (history_len <= 0 || slot < 0 || slot >= history_len || margin < -126 || margin > 127) return FP8_ERR_INVALID_ARG;
+  fp8_status_t st = check_quant_shape(rows, cols, FP8_GRAN_TENSOR);
+  if (st != FP8_OK) return st;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (x_dev == nullptr || q_dev == nullptr || scale_dev == nullptr || amax_history_dev == nullptr)
+    return FP8_ERR_INVALID_ARG;
+  if (ld_x < cols || ld_q < cols) return FP8_ERR_INVALID_ARG;
+  if (!aligned(x_dev, 16) || !aligned(q_dev, 16) || ld_x % 8 || ld_q % 16) return FP8_ERR_ALIGNMENT;
+  if (!aligned(scale_dev, 4) || !aligned(amax_history_dev, 4)) return FP8_ERR_ALIGNMENT;
+  return launch_quantize_delayed(static_cast<const uint16_t *>(x_dev), rows, cols, ld_x, fmt, amax_history_dev,
+                                 history_len, slot, margin, static_cast<uint8_t *>(q_dev), ld_q, scale_dev,
+                                 reinterpret_cast<cudaStream_t>(stream));
 }
 
 fp8_status_t fp8_dequantize(const void *q_dev, int64_t rows, int64_t cols, int64_t ld_q, fp8_format_t fmt,
@@ -219,6 +240,24 @@ fp8_status_t fp8_gemm_blockscaled(const void *a_dev, const float *a_scales_dev, 
   return launch_gemm_epilogue_scaled(static_cast<const uint8_t *>(a_dev), a_scales_dev, a_gran == FP8_GRAN_TOKEN,
                                      static_cast<const uint8_t *>(b_dev), b_scales_dev, b_gran == FP8_GRAN_TOKEN,
                                      a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status, s);
+}
+
+fp8_status_t fp8_gemm_blockscaled_quantized_out(const void *a_dev, const float *a_scales_dev, const void *b_dev,
+                                                const float *b_scales_dev, fp8_format_t a_fmt, fp8_format_t b_fmt,
+                                                fp8_format_t out_fmt, void *q_out_dev, float *q_scales_dev,
+                                                int64_t M, int64_t N, int64_t K, int *dev_status,
+                                                fp8_stream_t stream) {
+  if (!valid_fmt(out_fmt)) return FP8_ERR_INVALID_ARG;
+  fp8_status_t st = check_gemm_common(a_dev, b_dev, q_out_dev, M, N, K, a_fmt, b_fmt);
+  if (st != FP8_OK || M == 0 || N == 0) return st;
+  if (K % 128 != 0 || N % 128 != 0) return FP8_ERR_UNSUPPORTED_SHAPE;
+  if (a_scales_dev == nullptr || b_scales_dev == nullptr || q_scales_dev == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(a_scales_dev, 4) || !aligned(b_scales_dev, 4) || !aligned(q_scales_dev, 4)) return FP8_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return FP8_ERR_ALIGNMENT;
+  return launch_gemm_fold_quantized(static_cast<const uint8_t *>(a_dev), a_scales_dev,
+                                    static_cast<const uint8_t *>(b_dev), b_scales_dev, a_fmt, b_fmt, out_fmt,
+                                    static_cast<uint8_t *>(q_out_dev), q_scales_dev, M, N, K, dev_status,
+                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,

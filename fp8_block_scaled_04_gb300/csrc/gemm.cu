@@ -31,12 +31,18 @@
 #include <stdint.h>
 
 #include "internal.h"
+#include "fp8_math.cuh"
 #include "ptx.cuh"
 
 namespace fp8bs {
 namespace {
 
 constexpr int BM = 128;  // tile rows (MMA M)
+#ifndef MX_BN
+#define MX_BN 128      // MXFP8 tile width
+#define MX_STAGES 6
+#define MX_NACC 2
+#endif
 constexpr int BK = 128;  // K per stage (bytes of FP8)
 
 struct SharedCtl {
@@ -72,6 +78,18 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
   }
 }
 
+#ifndef FOLD_CHUNK
+#define FOLD_CHUNK 16  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
+#endif
+
+// acc[base + i] += sc * (r[2i], r[2i+1]) for i < CH/2, as packed fp32x2 FMAs.
+template <int CH>
+__device__ __forceinline__ void fold_chunk(float2 (&acc)[64], int base, float2 sc2, const uint32_t (&r)[CH]) {
+#pragma unroll
+  for (int i = 0; i < CH / 2; ++i)
+    acc[base + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), acc[base + i]);
+}
+
 // Producer drain after an abort: wait (bounded) for the copies of the last
 // in-flight iterations so that no TMA write lands after the CTA exits.
 template <int STAGES>
@@ -90,22 +108,46 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int &mt, int &n
 // =====================================================================
 // Fold kernel: 1x128 x 128x128 scales, per-chunk fp32 fold in registers
 // =====================================================================
+// Warp layout (12 warps): warpgroup 0 = producer (warp 0), MMA issuer and
+// tensor-memory owner (warp 1), two idle warps; warpgroups 1-2 = fold warps.
+// The fold warps keep 128 fp32 accumulators each and get most of the register
+// file (setmaxnreg), the other warpgroup gives registers back.
 template <int BN, int STAGES>
 struct FoldCfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int CONSUMER_WARPS = 4 * (BN / 128);  // each thread folds 128 columns of one row
-  static constexpr int THREADS = 64 + 32 * CONSUMER_WARPS;
+  static constexpr int FIRST_CONSUMER_WARP = 4;
+  static constexpr int THREADS = 32 * (FIRST_CONSUMER_WARP + CONSUMER_WARPS);
   static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  // setmaxnreg budgets. The increases are served from the registers the CTA
+  // was launched with (registers per thread x THREADS), so the split must fit
+  // in that pool or the increase never completes; launch_fold_tiles checks it
+  // against the compiled register count before launching.
+  static constexpr uint32_t REGS_CONTROL = 40;
+  static constexpr uint32_t REGS_FOLD = BN == 256 ? 224 : 240;
+  static constexpr uint32_t REGS_NEEDED = REGS_CONTROL * 32 * FIRST_CONSUMER_WARP + REGS_FOLD * 32 * CONSUMER_WARPS;
 };
 
-template <int BN, int STAGES>
+// True when the kernel's launch register pool covers the setmaxnreg split.
+template <typename KernelT>
+bool reg_split_fits(KernelT kernel, int threads, uint32_t needed) {
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return false;
+  return static_cast<uint64_t>(attr.numRegs) * static_cast<uint64_t>(threads) >= needed;
+}
+
+// QFMT < 0: bf16 output. QFMT = FP8_E4M3 / FP8_E5M2: the epilogue quantizes
+// its own bf16-rounded output with 1x128 scales (the next layer's activation
+// format) and writes codes + scales instead of bf16.
+template <int BN, int STAGES, int QFMT>
 __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     gemm_fold_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out, int M,
-                     int N, int K, uint32_t idesc, int *dev_status) {
+                     const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
+                     uint8_t *__restrict__ q_out, float *__restrict__ q_scales, int M, int N, int K, uint32_t idesc,
+                     int *dev_status) {
   using C = FoldCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -144,8 +186,9 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < C::FIRST_CONSUMER_WARP) {
+    regs_dealloc<C::REGS_CONTROL>();
+    if (warp == 0 && lane == 0) {
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -167,9 +210,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
         flag_abort(&ctl, dev_status);
         drain_stages<STAGES>(full, it);
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
       int it = 0, kc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -197,14 +238,15 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
       mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
     }
   } else {
+    regs_alloc<C::REGS_FOLD>();
     // ------------------------------------------------ fold consumers
-    const int cw = warp - 2;
+    const int cw = warp - C::FIRST_CONSUMER_WARP;
     const int quarter = warp & 3;  // tensor-memory lanes this warp may access
     const int half = cw >> 2;      // which 128-column half of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     int kc = 0;
     bool ok = true;
-    float acc[128];
+    float2 acc[64];
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, num_m, mt, nt);
@@ -215,7 +257,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
       const float *sa_row = sa + m;
       const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
       // scale prefetch, two chunks ahead
       float sa0 = row_ok ? __ldg(sa_row) : 0.0f;
       float sb0 = col_ok ? __ldg(sb_blk) : 0.0f;
@@ -232,34 +274,285 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
         }
         tc_fence_after();
         const float sc = sa0 * sb0;
-        const uint32_t col = static_cast<uint32_t>(b * BN + half * 128);
+        const float2 sc2 = make_float2(sc, sc);
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BN + half * 128);
+        constexpr int CH = FOLD_CHUNK, NCH = 128 / FOLD_CHUNK;
+        if constexpr (CH >= 64) {
+          // few large loads, one round trip each: load, wait, fold
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(tmem + lane_base + col + 16 * c, r);
-          tmem_wait_ld();
+          for (int c = 0; c < NCH; ++c) {
+            uint32_t rb[CH];
+            tmem_ld_chunk<CH>(taddr + CH * c, rb);
+            tmem_wait_ld_regs(rb);
+            if (c + 1 == NCH) {
+              // every load of this buffer has landed: hand it back to the MMA warp
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[b]);
+            }
+            fold_chunk<CH>(acc, c * (CH / 2), sc2, rb);
+          }
+        } else {
+          // two chunk buffers: the load of chunk c+1 is in flight while chunk c
+          // folds; the fold is packed fp32x2 FMA (two IEEE fmas per instruction)
+          uint32_t rbuf[2][CH];
+          tmem_ld_chunk<CH>(taddr, rbuf[0]);
+          tmem_wait_ld_regs(rbuf[0]);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(sc, __uint_as_float(r[i]), acc[16 * c + i]);
+          for (int c = 0; c < NCH; ++c) {
+            if (c + 1 < NCH) tmem_ld_chunk_keep<CH>(taddr + CH * (c + 1), rbuf[(c + 1) & 1], rbuf[c & 1]);
+            fold_chunk<CH>(acc, c * (CH / 2), sc2, rbuf[c & 1]);
+            if (c + 1 < NCH) {
+              tmem_wait_ld_regs(rbuf[(c + 1) & 1]);
+              if (c + 2 == NCH) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+              }
+            }
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
         sa0 = sa1;
         sb0 = sb1;
         sa1 = sa2;
         sb1 = sb2;
       }
       if (!ok) break;
-      // epilogue: bf16 out, straight from registers
+      // epilogue, straight from registers
       if (row_ok) {
         const int n0 = nb * 128;
-        uint16_t *dst = out + static_cast<int64_t>(m) * N + n0;
+        if constexpr (QFMT < 0) {
+          uint16_t *dst = out + static_cast<int64_t>(m) * N + n0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
+          for (int j = 0; j < 16; ++j) {  // 8 columns (16 bytes of bf16) per store
+            if (8 * j < N - n0) {
+              const uint4 w =
+                  make_uint4(pack_bf16x2(acc[4 * j].x, acc[4 * j].y), pack_bf16x2(acc[4 * j + 1].x, acc[4 * j + 1].y),
+                             pack_bf16x2(acc[4 * j + 2].x, acc[4 * j + 2].y),
+                             pack_bf16x2(acc[4 * j + 3].x, acc[4 * j + 3].y));
+              *reinterpret_cast<uint4 *>(dst + 8 * j) = w;
+            }
+          }
+        } else if (n0 < N) {
+          // this thread's 128 columns are exactly one 1x128 group of the output row:
+          // round to bf16 (the unfused output), amax, scale, encode
+          uint32_t mx = 0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = acc[32 * c + i];
-          store_row32(dst + 32 * c, v, N - n0 - 32 * c);
+          for (int i = 0; i < 64; ++i) {
+            const uint32_t p = pack_bf16x2(acc[i].x, acc[i].y);
+            acc[i] = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
+            mx = max(mx, max(p & 0x7fffu, (p >> 16) & 0x7fffu));
+          }
+          float s, s_inv;
+          scale_pair(__uint_as_float(mx << 16), vmax_of(QFMT), s, s_inv);
+          q_scales[static_cast<int64_t>(n0 >> 7) * M + m] = s;
+          uint8_t *qdst = q_out + static_cast<int64_t>(m) * N + n0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {  // 16 codes per store
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              f[2 * i] = acc[8 * j + i].x;
+              f[2 * i + 1] = acc[8 * j + i].y;
+            }
+            const uint2 lo = encode8<QFMT>(reinterpret_cast<const float(&)[8]>(f[0]), s_inv);
+            const uint2 hi = encode8<QFMT>(reinterpret_cast<const float(&)[8]>(f[8]), s_inv);
+            *reinterpret_cast<uint4 *>(qdst + 16 * j) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) flag_abort(&ctl, dev_status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// =====================================================================
+// Fold kernel, operands swapped for few activation rows (decode shapes)
+// =====================================================================
+// D[n, m] = sum_k W[n, k] X[m, k]: the MMA's M side is 128 rows of W (one
+// 128x128 weight block per K chunk, so one weight scale per chunk), its N side
+// is BX rows of X. Each fold thread owns one W row and BX accumulators; the
+// activation scales s_x[kb, m] vary along its row and are broadcast by shuffles.
+template <int BX, int STAGES>
+struct SwapCfg {
+  static constexpr int W_BYTES = BM * BK;
+  static constexpr int X_BYTES = BX * BK;
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+  static constexpr int NBUF = 4;                       // tensor-memory partial buffers
+  static constexpr int THREADS = 32 * (2 + 4);
+  static constexpr uint32_t TMEM_COLS = NBUF * BX <= 32 ? 32 : (NBUF * BX <= 64 ? 64 : (NBUF * BX <= 128 ? 128 : 256));
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  static_assert(BX % 16 == 0 && BX <= 64, "MMA N side");
+};
+
+template <int BX, int STAGES>
+__global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
+    gemm_fold_swap_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                          const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
+                          int M, int N, int K, uint32_t idesc, int *dev_status) {
+  using C = SwapCfg<BX, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[C::NBUF], tempty[C::NBUF], drain;
+  __shared__ SharedCtl ctl;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = K / BK;
+  const int num_x = (M + BX - 1) / BX;
+  const int num_w = (N + BM - 1) / BM;
+  const int ntiles = num_x * num_w;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < C::NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(&drain, 1);
+    ctl.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int wt = tile / num_x, xt = tile - wt * num_x;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t *w_s = smem + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(w_s, &tmW, kb * BK, wt * BM, &full[s]);
+          tma_load_2d(w_s + C::W_BYTES, &tmX, kb * BK, xt * BX, &full[s]);
+        }
+      }
+      if (!ok) {
+        flag_abort(&ctl, dev_status);
+        drain_stages<STAGES>(full, it);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, kc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+          const int b = kc % C::NBUF;
+          const int s = it % STAGES;
+          if (!mbar_wait(&tempty[b], ((kc / C::NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
+              !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t x0 = w0 + C::W_BYTES;
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8f6f4(d, sdesc_k_sw128(w0 + 32 * k), sdesc_k_sw128(x0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          tc_commit(&tfull[b]);
+        }
+      }
+      if (!ok) flag_abort(&ctl, dev_status);
+      tc_commit(&drain);
+      mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    constexpr int XR = (BX + 31) / 32;  // activation-scale registers per lane
+    int kc = 0;
+    bool ok = true;
+    float acc[BX];
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const int wt = tile / num_x, xt = tile - wt * num_x;
+      const int n = wt * BM + quarter * 32 + lane;  // this thread's W row / output column
+      const int m0 = xt * BX;
+      const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
+#pragma unroll
+      for (int j = 0; j < BX; ++j) acc[j] = 0.0f;
+      // lane l holds s_x[kb, m0 + 32 r + l]; prefetched two chunks ahead
+      float x0[XR], x1[XR], x2[XR];
+      auto load_sx = [&](int kbq, float (&dst)[XR]) {
+#pragma unroll
+        for (int r = 0; r < XR; ++r) {
+          const int mm = m0 + 32 * r + lane;
+          dst[r] = (kbq < KB && 32 * r + lane < BX && mm < M) ? __ldg(sa + static_cast<int64_t>(kbq) * M + mm) : 0.0f;
+        }
+      };
+      load_sx(0, x0);
+      load_sx(1, x1);
+      float w0 = __ldg(sb_blk), w1 = KB > 1 ? __ldg(sb_blk + 1) : 0.0f;
+      for (int kb = 0; kb < KB; ++kb, ++kc) {
+        const int b = kc % C::NBUF;
+        load_sx(kb + 2, x2);
+        const float w2 = kb + 2 < KB ? __ldg(sb_blk + kb + 2) : 0.0f;
+        const bool got = mbar_wait(&tfull[b], (kc / C::NBUF) & 1, kWaitTimeoutNs, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
+#pragma unroll
+        for (int c = 0; c < BX / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + 16 * c, r);
+          tmem_wait_ld_regs(r);
+          if (c == BX / 16 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = 16 * c + i;
+            const float sx = __shfl_sync(0xffffffffu, x0[j / 32], j % 32);
+            acc[j] = fmaf(w0 * sx, __uint_as_float(r[i]), acc[j]);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < XR; ++r) {
+          x0[r] = x1[r];
+          x1[r] = x2[r];
+        }
+        w0 = w1;
+        w1 = w2;
+      }
+      if (!ok) break;
+      if (n < N) {
+#pragma unroll
+        for (int j = 0; j < BX; ++j) {
+          const int m = m0 + j;
+          if (m < M) out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
         }
       }
     }
@@ -278,7 +571,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
 // Tensor-memory accumulating kernel: epilogue-scaled (MX = false) or
 // block-scaled MXFP8 (MX = true)
 // =====================================================================
-template <bool MX, int BN, int STAGES>
+template <bool MX, int BN, int STAGES, int NACC>
 struct AccCfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
@@ -289,22 +582,22 @@ struct AccCfg {
   static constexpr int CONSUMER_WARPS = 4 * (BN / 128);
   static constexpr int THREADS = 64 + 32 * CONSUMER_WARPS;
   static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;  // tensor-memory columns per stage
-  static constexpr int ACC_COLS = 2 * BN;                       // two accumulators
+  static constexpr int ACC_COLS = NACC * BN;                    // NACC accumulators (2: epilogue overlaps MMA)
   static constexpr uint32_t TMEM_COLS = ACC_COLS + STAGES * SF_COLS <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_STRIDE + 1024;
   static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory budget");
 };
 
-template <bool MX, int BN, int STAGES>
-__global__ void __launch_bounds__(AccCfg<MX, BN, STAGES>::THREADS, 1)
+template <bool MX, int BN, int STAGES, int NACC>
+__global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
     gemm_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float *__restrict__ sa, int sa_per_row, const float *__restrict__ sb, int sb_per_col,
                      const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ out,
                      int M, int N, int K, uint32_t idesc, int *dev_status) {
-  using C = AccCfg<MX, BN, STAGES>;
+  using C = AccCfg<MX, BN, STAGES, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  __shared__ uint64_t full[STAGES], empty[STAGES], afull[2], aempty[2], drain;
+  __shared__ uint64_t full[STAGES], empty[STAGES], afull[NACC], aempty[NACC], drain;
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -319,7 +612,7 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES>::THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       mbar_init(&afull[b], 1);
       mbar_init(&aempty[b], C::CONSUMER_WARPS);
     }
@@ -380,8 +673,8 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES>::THREADS, 1)
       bool ok = true;
       const uint32_t sf_col0 = static_cast<uint32_t>(C::ACC_COLS);
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tc) {
-        const int b = tc & 1;
-        if (!mbar_wait(&aempty[b], ((tc >> 1) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+        const int b = tc % NACC;
+        if (!mbar_wait(&aempty[b], ((tc / NACC) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
           ok = false;
           break;
         }
@@ -435,11 +728,11 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES>::THREADS, 1)
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
       int mt, nt;
       tile_coords(tile, num_m, mt, nt);
-      const int b = tc & 1;
+      const int b = tc % NACC;
       const int m = mt * BM + quarter * 32 + lane;
       const bool row_ok = m < M;
       const int n0 = nt * BN + half * 128;
-      const bool got = mbar_wait(&afull[b], (tc >> 1) & 1, kWaitTimeoutNs, &ctl.abort);
+      const bool got = mbar_wait(&afull[b], (tc / NACC) & 1, kWaitTimeoutNs, &ctl.abort);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -520,11 +813,28 @@ int persistent_grid(int ntiles) {
   return ntiles < sms ? ntiles : sms;
 }
 
-}  // namespace
-
-fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+template <int BX, int ST>
+fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
                               cudaStream_t stream) {
+  using C = SwapCfg<BX, ST>;
+  CUtensorMap tx, tw;
+  if (!make_tmap_u8(&tx, a, M, K, K, BX, BK) || !make_tmap_u8(&tw, b, N, K, K, BM, BK)) return FP8_ERR_CUDA;
+  auto kern = gemm_fold_swap_kernel<BX, ST>;
+  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+  const int ntiles = static_cast<int>(((M + BX - 1) / BX) * ((N + BM - 1) / BM));
+  // the MMA's A operand is W (format b_fmt), its B operand is X (a_fmt)
+  kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(tx, tw, sa, sb, out, static_cast<int>(M),
+                                                                 static_cast<int>(N), static_cast<int>(K),
+                                                                 idesc_f8f6f4(b_fmt, a_fmt, BM, BX), dev_status);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int QFMT>
+fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+                               int b_fmt, uint16_t *out, uint8_t *q_out, float *q_scales, int64_t M, int64_t N,
+                               int64_t K, int *dev_status, cudaStream_t stream) {
   // Wide tiles when there are enough of them to fill the GPU, else 128-wide.
   const int sms = device_sm_count();
   const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
@@ -535,35 +845,57 @@ fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *
     constexpr int BN = 256, ST = 4;
     using C = FoldCfg<BN, ST>;
     if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-    auto kern = gemm_fold_kernel<BN, ST>;
-    if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+    auto kern = gemm_fold_kernel<BN, ST, QFMT>;
+    if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
     const int ntiles = static_cast<int>(tiles256);
     kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-        ta, tb, sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        ta, tb, sa, sb, out, q_out, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
   } else {
     constexpr int BN = 128, ST = 6;
     using C = FoldCfg<BN, ST>;
     if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-    auto kern = gemm_fold_kernel<BN, ST>;
-    if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+    auto kern = gemm_fold_kernel<BN, ST, QFMT>;
+    if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
     const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + 127) / 128));
     kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-        ta, tb, sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        ta, tb, sa, sb, out, q_out, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
   }
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
+}  // namespace
+
+fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+                              int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
+                              cudaStream_t stream) {
+  // Few activation rows (decode): swap operands so the 128-row MMA side is W.
+  if (M <= 16) return launch_fold_swap<16, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
+  if (M <= 32) return launch_fold_swap<32, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
+  if (M <= 64) return launch_fold_swap<64, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
+  return launch_fold_tiles<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
+}
+
+fp8_status_t launch_gemm_fold_quantized(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
+                                        int a_fmt, int b_fmt, int out_fmt, uint8_t *q_out, float *q_scales,
+                                        int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {
+  if (out_fmt == FP8_E4M3)
+    return launch_fold_tiles<FP8_E4M3>(a, sa, b, sb, a_fmt, b_fmt, nullptr, q_out, q_scales, M, N, K, dev_status,
+                                       stream);
+  return launch_fold_tiles<FP8_E5M2>(a, sa, b, sb, a_fmt, b_fmt, nullptr, q_out, q_scales, M, N, K, dev_status,
+                                     stream);
+}
+
 fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool a_token, const uint8_t *b,
                                          const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,
                                          int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {
-  constexpr int BN = 256, ST = 4;
-  using C = AccCfg<false, BN, ST>;
+  constexpr int BN = 256, ST = 4, NACC = 2;
+  using C = AccCfg<false, BN, ST, NACC>;
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-  auto kern = gemm_tmem_kernel<false, BN, ST>;
+  auto kern = gemm_tmem_kernel<false, BN, ST, NACC>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
@@ -576,11 +908,11 @@ fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool
 fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb, int a_fmt,
                             int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
                             cudaStream_t stream) {
-  constexpr int BN = 128, ST = 6;
-  using C = AccCfg<true, BN, ST>;
+  constexpr int BN = MX_BN, ST = MX_STAGES, NACC = MX_NACC;
+  using C = AccCfg<true, BN, ST, NACC>;
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-  auto kern = gemm_tmem_kernel<true, BN, ST>;
+  auto kern = gemm_tmem_kernel<true, BN, ST, NACC>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(

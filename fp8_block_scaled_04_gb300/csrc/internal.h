@@ -31,6 +31,10 @@ fp8_status_t launch_quantize_tensor_noalloc(const uint16_t *x, int64_t rows, int
                                             cudaStream_t stream);
 size_t noalloc_scratch_capacity();
 
+fp8_status_t launch_quantize_delayed(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                     float *history, int hlen, int slot, int margin, uint8_t *q, int64_t ld_q,
+                                     float *scale_out, cudaStream_t stream);
+
 fp8_status_t launch_encode_f32(const float *x, int64_t n, int fmt, uint8_t *out, cudaStream_t stream);
 
 fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, int fmt, int gran,
@@ -43,6 +47,10 @@ enum class EpiScale : int { kTensorTensor = 0, kTensorToken = 1, kTokenTensor = 
 fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
                               cudaStream_t stream);
+
+fp8_status_t launch_gemm_fold_quantized(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
+                                        int a_fmt, int b_fmt, int out_fmt, uint8_t *q_out, float *q_scales,
+                                        int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream);
 
 fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool a_token, const uint8_t *b,
                                          const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,

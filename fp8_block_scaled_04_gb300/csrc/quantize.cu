@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "fp8_math.cuh"
 #include "ptx.cuh"
 
 namespace fp8bs {
@@ -40,62 +41,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   return v;
 }
 
-__device__ __forceinline__ float vmax_of(int fmt) { return fmt == FP8_E4M3 ? 448.0f : 57344.0f; }
-
-// max |x| of eight bf16 (as the 15-bit magnitude pattern, which orders like the value)
-__device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
-  const uint32_t m = 0x7fff7fffu;
-  uint32_t a = __vmaxu2(__vmaxu2(v.x & m, v.y & m), __vmaxu2(v.z & m, v.w & m));
-  return max(a & 0xffffu, a >> 16);
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(uint4 v, float (&f)[8]) {
-  f[0] = __uint_as_float(v.x << 16);
-  f[1] = __uint_as_float(v.x & 0xffff0000u);
-  f[2] = __uint_as_float(v.y << 16);
-  f[3] = __uint_as_float(v.y & 0xffff0000u);
-  f[4] = __uint_as_float(v.z << 16);
-  f[5] = __uint_as_float(v.z & 0xffff0000u);
-  f[6] = __uint_as_float(v.w << 16);
-  f[7] = __uint_as_float(v.w & 0xffff0000u);
-}
-
-__device__ __forceinline__ void scale_pair(float amax, float vmax, float &s, float &s_inv) {
-  s = __fdiv_rn(amax, vmax);
-  s_inv = __frcp_rn(s);
-  if (s == 0.0f || !isfinite(s_inv)) s_inv = 0.0f;
-}
-
-// ceil(log2(fp32(amax / vmax))) from the bits, clamped to UE8M0's range.
-__device__ __forceinline__ int mx_shared_exponent(float amax, float vmax) {
-  const uint32_t u = __float_as_uint(__fdiv_rn(amax, vmax)) & 0x7fffffffu;
-  if (u == 0) return -127;
-  if (u >= 0x7f800000u) return 127;
-  const uint32_t ex = u >> 23, fr = u & 0x7fffffu;
-  int e;
-  if (ex != 0)
-    e = static_cast<int>(ex) - 127 + (fr != 0 ? 1 : 0);
-  else
-    e = (31 - __clz(fr)) - 149 + ((fr & (fr - 1u)) != 0 ? 1 : 0);
-  return min(127, max(-127, e));
-}
-
-// 2^p exactly, p in [-127, 127]
-__device__ __forceinline__ float exp2_exact(int p) {
-  return p >= -126 ? __uint_as_float(static_cast<uint32_t>(p + 127) << 23) : __uint_as_float(0x00400000u);
-}
-
-template <int FMT>
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s_inv) {
-  float y[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(f[i], s_inv);
-  uint32_t p[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = FMT == FP8_E4M3 ? cvt_e4m3x2(y[2 * i], y[2 * i + 1]) : cvt_e5m2x2(y[2 * i], y[2 * i + 1]);
-  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-}
-
 __device__ __forceinline__ int64_t mx_tiled_index(int64_t r, int64_t j, int64_t ngroups) {
   const int64_t col_blocks = (ngroups + 3) >> 2;
   return (((r >> 7) * col_blocks + (j >> 2)) << 9) + ((r & 31) << 4) + (((r & 127) >> 5) << 2) + (j & 3);
@@ -103,12 +48,23 @@ __device__ __forceinline__ int64_t mx_tiled_index(int64_t r, int64_t j, int64_t 
 
 // ------------------------------------------------------------ group kernels
 // GROUP elements share a scale (128: 1x128 tile, 32: MX). A warp task is one
-// row segment of kSegVec vectors; groups never straddle rows or lanes.
+// row segment of kSegVec vectors (4 slots of 32 lanes x 8 elements); groups
+// never straddle rows or lanes. The per-group scale arithmetic (an IEEE
+// division and reciprocal, or the MX exponent) is done once per group: lanes
+// take one (slot, group) pair each, then hand the results back by shuffles.
+template <int v>
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&m)[4], int i) {
+  return i == 0 ? m[0] : (i == 1 ? m[1] : (i == 2 ? m[2] : m[3]));
+}
+
 template <int FMT, int GROUP, bool MX, bool TILED>
 __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
                                                                int64_t ldq, void *__restrict__ scales) {
-  constexpr int TPG = GROUP / 8;
+  constexpr int TPG = GROUP / 8;            // lanes per group
+  constexpr int GPS = 32 / TPG;             // groups per slot (2 for 1x128, 8 for MX)
+  constexpr int PAIRS = kVecPerLane * GPS;  // (slot, group) pairs per task: 8 or 32
+  static_assert(PAIRS <= 32, "one pair per lane");
   const int lane = threadIdx.x & 31;
   const int64_t vec_per_row = cols >> 3;
   const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
@@ -116,6 +72,9 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
   const float vmax = vmax_of(FMT);
+  // the pair this lane computes the scale of
+  const int p_slot = lane % kVecPerLane;
+  const int p_grp = (lane / kVecPerLane) % GPS;
   for (int64_t t = warp0; t < tasks; t += nwarps) {
     const int64_t r = t / segs;
     const int64_t cv0 = (t - r * segs) * kSegVec;
@@ -125,31 +84,41 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
       const int64_t cv = cv0 + i * 32 + lane;
       v[i] = cv < vec_per_row ? ld_stream_v4(x + r * ldx + cv * 8) : make_uint4(0, 0, 0, 0);
     }
+    uint32_t m[kVecPerLane];
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i) {
-      const int64_t cv = cv0 + i * 32 + lane;
-      uint32_t m = absmax_bits8(v[i]);
+      m[i] = absmax_bits8(v[i]);
 #pragma unroll
-      for (int o = TPG / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const float amax = __uint_as_float(m << 16);
+      for (int o = TPG / 2; o > 0; o >>= 1) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+    }
+    // scale of pair (p_slot, p_grp): every lane of group p_grp holds that group's
+    // amax for every slot; lane p_grp * TPG + p_slot offers slot p_slot's value
+    const uint32_t pm = __shfl_sync(0xffffffffu, pick4<0>(m, p_slot), p_grp * TPG + p_slot);
+    const float amax = __uint_as_float(pm << 16);
+    const int64_t pcv = cv0 + p_slot * 32 + p_grp * TPG;  // first vector of the pair's group
+    float my_inv;
+    if (MX) {
+      const int e = mx_shared_exponent(amax, vmax);
+      my_inv = exp2_exact(-e);
+      if (lane < PAIRS && pcv < vec_per_row) {
+        const int64_t j = pcv / TPG;
+        const int64_t ng = cols / 32;
+        uint8_t *sf = static_cast<uint8_t *>(scales);
+        sf[TILED ? mx_tiled_index(r, j, ng) : r * ng + j] = static_cast<uint8_t>(e + 127);
+      }
+    } else {
+      float s;
+      scale_pair(amax, vmax, s, my_inv);
+      if (lane < PAIRS && pcv < vec_per_row) static_cast<float *>(scales)[(pcv / TPG) * rows + r] = s;
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      // pair (slot i, this lane's group) was computed by lane group * kVecPerLane + i
+      const float s_inv = __shfl_sync(0xffffffffu, my_inv, (lane / TPG) * kVecPerLane + i);
+      const int64_t cv = cv0 + i * 32 + lane;
       if (cv >= vec_per_row) continue;
       float f[8];
       bf16x8_to_f32(v[i], f);
-      float s_inv;
-      if (MX) {
-        const int e = mx_shared_exponent(amax, vmax);
-        s_inv = exp2_exact(-e);
-        if ((lane & (TPG - 1)) == 0) {
-          const int64_t j = cv / TPG;
-          const int64_t ng = cols / 32;
-          uint8_t *sf = static_cast<uint8_t *>(scales);
-          sf[TILED ? mx_tiled_index(r, j, ng) : r * ng + j] = static_cast<uint8_t>(e + 127);
-        }
-      } else {
-        float s;
-        scale_pair(amax, vmax, s, s_inv);
-        if ((lane & (TPG - 1)) == 0) static_cast<float *>(scales)[(cv / TPG) * rows + r] = s;
-      }
       *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
     }
   }
@@ -194,12 +163,15 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restri
 
 // Pass 2: encode with one scale; the scale comes from the amax of pass 1 or
 // from the caller (static scaling).
+// record_amax (nullable): also reduce this tensor's amax into *record_amax
+// (fp32 bits, atomicMax) -- the history update of delayed scaling.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) quant_tensor_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                 int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
                                                                 int64_t ldq, float *__restrict__ scale_out,
                                                                 const uint32_t *__restrict__ amax_bits,
-                                                                const float *__restrict__ static_scale) {
+                                                                const float *__restrict__ static_scale,
+                                                                uint32_t *__restrict__ record_amax = nullptr) {
   float s, s_inv;
   if (static_scale != nullptr) {
     s = *static_scale;
@@ -208,14 +180,16 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_kernel(const uint16_t *
   } else {
     scale_pair(__uint_as_float(*amax_bits), vmax_of(FMT), s, s_inv);
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out != nullptr) *scale_out = s;
   const int lane = threadIdx.x & 31;
+  uint32_t rec = 0;
   const int64_t vec_per_row = cols >> 3;
   const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
   const int64_t tasks = rows * segs;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  for (int64_t t = warp0; t < tasks; t += nwarps) {
+  for (int64_t tt = warp0; tt < tasks; tt += nwarps) {
+    const int64_t t = tasks - 1 - tt;  // reverse of pass 1: its last rows are still in L2
     const int64_t r = t / segs;
     const int64_t cv0 = (t - r * segs) * kSegVec;
     uint4 v[kVecPerLane];
@@ -228,10 +202,68 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_kernel(const uint16_t *
     for (int i = 0; i < kVecPerLane; ++i) {
       const int64_t cv = cv0 + i * 32 + lane;
       if (cv >= vec_per_row) continue;
+      if (record_amax != nullptr) rec = max(rec, absmax_bits8(v[i]));
       float f[8];
       bf16x8_to_f32(v[i], f);
       *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
     }
+  }
+  if (record_amax != nullptr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rec = max(rec, __shfl_xor_sync(0xffffffffu, rec, o));
+    __shared__ uint32_t red[kThreads / 32];
+    if (lane == 0) red[threadIdx.x >> 5] = rec;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t b = 0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
+      atomicMax(record_amax, b << 16);
+    }
+  }
+}
+
+// ------------------------------------------------------------ delayed scaling
+// One CTA: s from the amax history (max over non-negative finite entries;
+// a non-finite entry or an all-zero history gives s = 1), then the slot the
+// current tensor's amax goes into is cleared for the encode kernel's atomicMax.
+__global__ void __launch_bounds__(kThreads) delayed_scale_kernel(float *__restrict__ history, int hlen, int slot,
+                                                                 int margin, int fmt, float *__restrict__ scale_out) {
+  uint32_t best = 0;
+  int bad = 0;
+  for (int i = threadIdx.x; i < hlen; i += kThreads) {
+    const uint32_t u = __float_as_uint(history[i]);
+    if ((u & 0x7fffffffu) >= 0x7f800000u)
+      bad = 1;
+    else if ((u >> 31) == 0)
+      best = max(best, u);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  __shared__ uint32_t rb[kThreads / 32];
+  __shared__ int rbad[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) {
+    rb[threadIdx.x >> 5] = best;
+    rbad[threadIdx.x >> 5] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    int any_bad = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      b = max(b, rb[w]);
+      any_bad |= rbad[w];
+    }
+    float s = 1.0f;
+    if (!any_bad && b != 0) {
+      const float scaled = __fmul_rn(__uint_as_float(b), exp2_exact(margin));  // 2^m * max(H), one rounding
+      s = __fdiv_rn(scaled, vmax_of(fmt));
+    }
+    *scale_out = s;
+    history[slot] = 0.0f;
   }
 }
 
@@ -343,6 +375,73 @@ __global__ void __launch_bounds__(kThreads) quant_block_kernel(const uint16_t *_
   }
 }
 
+// ------------------------------------------------------------ per-channel
+// One scale per column (two passes, like per-tensor). A CTA owns a strip of
+// kChanCols columns (256 threads x 8 columns) and a chunk of rows; each row of
+// the strip is one contiguous 4 KB segment, read with 16-byte loads, four rows
+// in flight per thread.
+constexpr int kChanCols = kThreads * 8;
+
+__global__ void __launch_bounds__(kThreads) channel_amax_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                int64_t cols, int64_t ldx, int64_t rows_per_cta,
+                                                                uint32_t *__restrict__ col_amax) {
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChanCols + threadIdx.x * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
+  const int64_t r1 = min(rows, r0 + rows_per_cta);
+  if (c0 >= cols) return;
+  uint32_t m2[4] = {0u, 0u, 0u, 0u};  // packed 16-bit magnitude maxima of column pairs
+  for (int64_t r = r0; r < r1; r += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = r + i < r1 ? ld_stream_v4(x + (r + i) * ldx + c0) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m2[0] = __vmaxu2(m2[0], v[i].x & 0x7fff7fffu);
+      m2[1] = __vmaxu2(m2[1], v[i].y & 0x7fff7fffu);
+      m2[2] = __vmaxu2(m2[2], v[i].z & 0x7fff7fffu);
+      m2[3] = __vmaxu2(m2[3], v[i].w & 0x7fff7fffu);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    atomicMax(col_amax + c0 + 2 * j, (m2[j] & 0xffffu) << 16);
+    atomicMax(col_amax + c0 + 2 * j + 1, m2[j] & 0xffff0000u);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) channel_quant_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                 int64_t cols, int64_t ldx, int64_t rows_per_cta,
+                                                                 const uint32_t *__restrict__ col_amax,
+                                                                 uint8_t *__restrict__ q, int64_t ldq,
+                                                                 float *__restrict__ scales) {
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChanCols + threadIdx.x * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
+  const int64_t r1 = min(rows, r0 + rows_per_cta);
+  if (c0 >= cols) return;
+  float s_inv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float s;
+    scale_pair(__uint_as_float(col_amax[c0 + j]), vmax_of(FMT), s, s_inv[j]);
+    if (blockIdx.y == 0) scales[c0 + j] = s;
+  }
+  for (int64_t r = r0; r < r1; r += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = r + i < r1 ? ld_stream_v4(x + (r + i) * ldx + c0) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (r + i >= r1) continue;
+      float f[8];
+      bf16x8_to_f32(v[i], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], s_inv[j]);
+      *reinterpret_cast<uint2 *>(q + (r + i) * ldq + c0) = encode8<FMT>(f, 1.0f);
+    }
+  }
+}
+
 // ------------------------------------------------------------ dequantize
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__restrict__ q, int64_t rows, int64_t cols,
@@ -377,6 +476,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__rest
         case FP8_GRAN_TOKEN: s = sf[r]; break;
         case FP8_GRAN_TILE_1x128: s = sf[(c >> 7) * rows + r]; break;
         case FP8_GRAN_BLOCK_128x128: s = sf[(r >> 7) * (cols >> 7) + (c >> 7)]; break;
+        case FP8_GRAN_CHANNEL: s = 1.0f; break;
         default: {
           const int64_t ng = cols >> 5;
           const uint8_t e = sb[sf_layout == FP8_SF_TCGEN05 ? mx_tiled_index(r, c >> 5, ng) : r * ng + (c >> 5)];
@@ -384,6 +484,9 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__rest
         }
       }
       const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      float sc[16];  // per-element scales (differ only for per-channel scaling)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sc[e] = gran == FP8_GRAN_CHANNEL ? sf[c + e] : s;
       uint32_t o[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -392,8 +495,8 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__rest
           const uint16_t pair = static_cast<uint16_t>(w[j] >> (16 * h));
           const uint32_t hx2 = FMT == FP8_E4M3 ? cvt_e4m3x2_to_f16x2(pair) : cvt_e5m2x2_to_f16x2(pair);
           const __half2 hh = *reinterpret_cast<const __half2 *>(&hx2);
-          const float lo = __fmul_rn(__low2float(hh), s);
-          const float hi = __fmul_rn(__high2float(hh), s);
+          const float lo = __fmul_rn(__low2float(hh), sc[4 * j + 2 * h]);
+          const float hi = __fmul_rn(__high2float(hh), sc[4 * j + 2 * h + 1]);
           const uint32_t blo = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
           const uint32_t bhi = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
           o[2 * j + h] = blo | (bhi << 16);
@@ -517,10 +620,50 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
       ++launches;
       break;
     }
+    case FP8_GRAN_CHANNEL: {
+      uint32_t *col_amax = static_cast<uint32_t *>(workspace);
+      if (cudaMemsetAsync(col_amax, 0, static_cast<size_t>(cols) * sizeof(uint32_t), stream) != cudaSuccess)
+        return FP8_ERR_CUDA;
+      const int64_t strips = (cols + kChanCols - 1) / kChanCols;
+      int64_t chunks = (static_cast<int64_t>(device_sm_count()) * 8 + strips - 1) / strips;
+      const int64_t max_chunks = (rows + 3) / 4;
+      if (chunks > max_chunks) chunks = max_chunks;
+      if (chunks < 1) chunks = 1;
+      int64_t rpc = (rows + chunks - 1) / chunks;
+      rpc = (rpc + 3) / 4 * 4;
+      chunks = (rows + rpc - 1) / rpc;
+      dim3 g(static_cast<unsigned>(strips), static_cast<unsigned>(chunks));
+      channel_amax_kernel<<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax);
+      if (e4)
+        channel_quant_kernel<FP8_E4M3><<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax, q, ld_q,
+                                                                   static_cast<float *>(scales));
+      else
+        channel_quant_kernel<FP8_E5M2><<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax, q, ld_q,
+                                                                   static_cast<float *>(scales));
+      launches += 2;
+      break;
+    }
     default:
       return FP8_ERR_INVALID_ARG;
   }
   note_launches(launches);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t launch_quantize_delayed(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                                     float *history, int hlen, int slot, int margin, uint8_t *q, int64_t ld_q,
+                                     float *scale_out, cudaStream_t stream) {
+  delayed_scale_kernel<<<1, kThreads, 0, stream>>>(history, hlen, slot, margin, fmt, scale_out);
+  const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
+  const int grid = stream_grid(tasks);
+  uint32_t *rec = reinterpret_cast<uint32_t *>(history + slot);
+  if (fmt == FP8_E4M3)
+    quant_tensor_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, nullptr, nullptr,
+                                                                 scale_out, rec);
+  else
+    quant_tensor_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, nullptr, nullptr,
+                                                                 scale_out, rec);
+  note_launches(2);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -55,13 +55,19 @@ typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
  *   TILE_1x128     float[cols/128][rows]            (rows contiguous)
  *   BLOCK_128x128  float[ceil(rows/128)][cols/128]
  *   MX32           uint8 UE8M0 (2^(b-127)), one per 32 consecutive elements
- *                  of a row, in the layout chosen by fp8_sf_layout_t. */
+ *                  of a row, in the layout chosen by fp8_sf_layout_t.
+ *   CHANNEL        float[cols] (one per column: per-channel scales of a
+ *                  [tokens x channels] tensor such as a K or V cache -- "FP8
+ *                  Serving" guide, Things to try; "FP8 Mixed-Precision
+ *                  Serving", FP8 KV Cache). Quantize/dequantize only; not a
+ *                  GEMM operand granularity (it does not factor out of a K sum). */
 typedef enum {
   FP8_GRAN_TENSOR = 0,
   FP8_GRAN_TOKEN = 1,
   FP8_GRAN_TILE_1x128 = 2,
   FP8_GRAN_BLOCK_128x128 = 3,
-  FP8_GRAN_MX32 = 4
+  FP8_GRAN_MX32 = 4,
+  FP8_GRAN_CHANNEL = 5
 } fp8_gran_t;
 
 /* MX scale-factor layouts.
@@ -94,7 +100,8 @@ const char *fp8_status_string(fp8_status_t status);
 size_t fp8_scales_bytes(int64_t rows, int64_t cols, fp8_gran_t gran, fp8_sf_layout_t sf_layout);
 
 /* Workspace bytes fp8_quantize needs: 256 for dynamic per-tensor scaling (the
- * grid-wide amax of the first pass lives there), 0 otherwise. */
+ * grid-wide amax of the first pass lives there), cols*4 rounded up to 256 for
+ * per-channel scaling (the column maxima of the first pass), 0 otherwise. */
 size_t fp8_quantize_workspace_bytes(int64_t rows, int64_t cols, fp8_gran_t gran);
 
 /* Dynamic (or static per-tensor) quantization of a bf16 matrix.
@@ -114,7 +121,7 @@ size_t fp8_quantize_workspace_bytes(int64_t rows, int64_t cols, fp8_gran_t gran)
  *   workspace    device scratch of fp8_quantize_workspace_bytes() bytes
  *                (may be NULL when that is 0); its contents are clobbered;
  *                concurrent calls must not share it.
- * Shape rules: cols % 16 == 0 (TENSOR, TOKEN), cols % 128 == 0 (TILE_1x128,
+ * Shape rules: cols % 16 == 0 (TENSOR, TOKEN, CHANNEL), cols % 128 == 0 (TILE_1x128,
  * BLOCK_128x128), cols % 32 == 0 (MX32). x_dev and q_dev 16-byte aligned,
  * ld_x % 8 == 0, ld_q % 16 == 0, scales_dev 4-byte aligned. */
 fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x, fp8_format_t fmt,
@@ -146,6 +153,23 @@ fp8_status_t fp8_quantize_tensor_noalloc(const void *x_dev, int64_t rows, int64_
                                          fp8_format_t fmt, void *q_dev, int64_t ld_q, float *scale_dev,
                                          fp8_stream_t stream);
 
+/* Per-tensor quantization with delayed scaling ("FP8 Mixed-Precision Serving",
+ * Delayed Scaling: rho = FP8MaxValue / (2^m * max(H)) over a rolling amax
+ * history H; "Low precision", NVIDIA's taxonomy: per-tensor, delayed). One
+ * pass over x instead of current scaling's two.
+ *   amax_history_dev  float[history_len] in device memory, owned by the caller,
+ *                     initialised to 0 (entries must be >= 0).
+ * The scale is s = fp32(fp32(2^margin * max(H)) / V_max) and x is encoded as
+ * RNE_satfinite(x * fp32(1/s)) (values beyond the history's range saturate);
+ * a history whose maximum is 0 or that holds inf/NaN gives s = 1. s goes to
+ * *scale_dev; afterwards history[slot] = amax(x) (the caller advances slot by
+ * one per step, modulo history_len). Rules: 0 <= slot < history_len,
+ * -126 <= margin <= 127, shape and alignment as fp8_quantize with
+ * FP8_GRAN_TENSOR. Two kernels, no workspace. */
+fp8_status_t fp8_quantize_delayed(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x, fp8_format_t fmt,
+                                  float *amax_history_dev, int32_t history_len, int32_t slot, int32_t margin,
+                                  void *q_dev, int64_t ld_q, float *scale_dev, fp8_stream_t stream);
+
 /* Dequantization ("07 -- The FP8 Family": x_hat = x_fp8 * s; "Low precision",
  * qdq_e4m3 listing: exact decode, then one fp32 multiply by s):
  * out = bf16_RN(fp32(decode(q) * s)). Same layouts and rules as fp8_quantize;
@@ -175,6 +199,22 @@ fp8_status_t fp8_gemm_blockscaled(const void *a_dev, const float *a_scales_dev, 
                                   const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
                                   fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N,
                                   int64_t K, int *dev_status, fp8_stream_t stream);
+
+/* The block-scaled GEMM (1x128 activation tiles x 128x128 weight blocks) with
+ * quantization fused into its epilogue ("Low precision", practice 4: fuse
+ * quantization into the producing kernel's epilogue -- the per-block amax and
+ * scaling run on data already in registers instead of costing a separate pass
+ * over HBM). Each 128-column group of an output row is rounded to bf16 (the
+ * value fp8_gemm_blockscaled would store), then quantized exactly as
+ * fp8_quantize does with FP8_GRAN_TILE_1x128: q_out_dev uint8 [M x N] codes in
+ * out_fmt and q_scales_dev float [N/128][M] -- the next layer's activation
+ * operand. No bf16 output is written. Rules: K % 128 == 0, N % 128 == 0, other
+ * rules as fp8_gemm_blockscaled. */
+fp8_status_t fp8_gemm_blockscaled_quantized_out(const void *a_dev, const float *a_scales_dev, const void *b_dev,
+                                                const float *b_scales_dev, fp8_format_t a_fmt, fp8_format_t b_fmt,
+                                                fp8_format_t out_fmt, void *q_out_dev, float *q_scales_dev,
+                                                int64_t M, int64_t N, int64_t K, int *dev_status,
+                                                fp8_stream_t stream);
 
 /* MXFP8 GEMM on the tensor core's block-scaled MMA ("Low precision",
  * microscaling: 32 consecutive elements share one UE8M0 scale, applied inside

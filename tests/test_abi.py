@@ -37,7 +37,7 @@ def test_status_strings(L):
 
 
 @pytest.mark.parametrize("rows,cols", [(1, 128), (130, 640), (300, 1024), (0, 128)])
-@pytest.mark.parametrize("gran", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("gran", [0, 1, 2, 3, 4, 5])
 def test_scales_bytes_match_oracle_layout(L, rows, cols, gran):
     layouts = [fb.SF_LINEAR, fb.SF_TCGEN05] if gran == fb.MX32 else [fb.SF_LINEAR]
     for lay in layouts:
@@ -84,6 +84,15 @@ def test_quantize_refusals(L):
     assert _q(L, ldq=136) == fb.ERR_ALIGNMENT
     assert _q(L, gran=0) == fb.ERR_WORKSPACE  # dynamic per-tensor needs workspace
     assert _q(L, gran=0, ws=A16, wsb=16) == fb.ERR_WORKSPACE
+    assert _q(L, gran=5) == fb.ERR_WORKSPACE  # per-channel needs cols*4 bytes of workspace
+    assert _q(L, gran=5, ws=A16, wsb=256) == fb.ERR_WORKSPACE  # 128 cols -> 512 bytes
+    assert fb.workspace_bytes(8, 128, fb.CHANNEL) == 512
+    d = L.fp8_quantize_delayed
+    assert d(A16, 8, 128, 128, 0, A16, 4, 4, 0, A16b, 128, A16, None) == fb.ERR_INVALID_ARG  # slot >= len
+    assert d(A16, 8, 128, 128, 0, A16, 4, 0, 200, A16b, 128, A16, None) == fb.ERR_INVALID_ARG  # margin
+    assert d(A16, 8, 128, 128, 0, None, 4, 0, 0, A16b, 128, A16, None) == fb.ERR_INVALID_ARG
+    assert d(A16, 8, 120, 128, 0, A16, 4, 0, 0, A16b, 128, A16, None) == fb.ERR_UNSUPPORTED_SHAPE
+    assert d(A16, 0, 128, 128, 0, A16, 4, 0, 0, A16b, 128, A16, None) == fb.OK
     assert fb.launch_count() == n0
 
 
@@ -108,6 +117,11 @@ def test_gemm_refusals(L):
     assert _g(L, ga=3, gb=2) == fb.ERR_INVALID_ARG  # not a valid scale pair
     assert _g(L, ga=2, gb=1) == fb.ERR_INVALID_ARG
     assert _g(L, ga=4, gb=4) == fb.ERR_INVALID_ARG  # MX has its own entry point
+    assert _g(L, ga=5, gb=0) == fb.ERR_INVALID_ARG  # per-channel scales do not factor out of K
+    qo = L.fp8_gemm_blockscaled_quantized_out
+    assert qo(A16, A16, A16b, A16, 0, 0, 0, A16, A16, 16, 144, 128, None, None) == fb.ERR_UNSUPPORTED_SHAPE
+    assert qo(A16, A16, A16b, A16, 0, 0, 3, A16, A16, 16, 128, 128, None, None) == fb.ERR_INVALID_ARG
+    assert qo(A16, A16, A16b, A16, 0, 0, 0, A16, None, 16, 128, 128, None, None) == fb.ERR_INVALID_ARG
     assert _g(L, fa=5) == fb.ERR_INVALID_ARG
     assert _g(L, n=24) == fb.ERR_UNSUPPORTED_SHAPE  # N % 16
     assert _g(L, k=144) == fb.ERR_UNSUPPORTED_SHAPE  # fold needs K % 128

@@ -14,7 +14,7 @@ from gpu_util import bf16_host, f32_bits, to_dev_bf16
 pytestmark = pytest.mark.gpu
 
 FMTS = [fb.E4M3, fb.E5M2]
-GRANS = [fb.TENSOR, fb.TOKEN, fb.TILE_1x128, fb.BLOCK_128x128, fb.MX32]
+GRANS = [fb.TENSOR, fb.TOKEN, fb.TILE_1x128, fb.BLOCK_128x128, fb.MX32, fb.CHANNEL]
 # ragged rows (not multiples of 128), several 128-wide column blocks, one long row
 SHAPES = [(1, 128), (17, 256), (130, 640), (300, 1024), (64, 8192), (3, 20480)]
 
@@ -137,3 +137,22 @@ def test_encode_every_fp32(fmt):
         assert bad == 0, "first mismatch at fp32 pattern 0x%08x" % first
         total_bad += bad
     assert total_bad == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(37, 256), (300, 1024), (2048, 4096)])
+def test_delayed_scaling_sequence_bit_exact(fmt, shape):
+    """Five steps through a 3-entry amax history with margin 1: codes, scale and
+    history match the oracle after every step."""
+    rows, cols = shape
+    hist_d = torch.zeros(3, dtype=torch.float32, device="cuda")
+    hist_o = np.zeros(3, np.float32)
+    for step in range(5):
+        sigma = [1.0, 2.0, 0.5, 8.0, 1.0][step]
+        x = synth.bf16_matrix(rows, cols, sigma, 600 + step, 700 + step, 0.01, 30.0)
+        q, s = fb.quantize_delayed(to_dev_bf16(x), fmt, hist_d, slot=step % 3, margin=1)
+        torch.cuda.synchronize()
+        oq, os_, hist_o = oracle.quantize_delayed(x, fmt, hist_o, slot=step % 3, margin=1)
+        assert np.array_equal(q.cpu().numpy(), oq), step
+        assert np.array_equal(f32_bits(s.cpu().numpy()), f32_bits(os_)), step
+        assert np.array_equal(f32_bits(hist_d.cpu().numpy()), f32_bits(hist_o)), step
