@@ -39,9 +39,9 @@ namespace {
 
 constexpr int BM = 128;  // tile rows (MMA M)
 #ifndef MX_BN
-#define MX_BN 128      // MXFP8 tile width
-#define MX_STAGES 6
-#define MX_NACC 2
+#define MX_BN 256      // MXFP8 tile width
+#define MX_STAGES 4
+#define MX_NACC 1      // one accumulator: tensor memory also holds the scale factors
 #endif
 constexpr int BK = 128;  // K per stage (bytes of FP8)
 
@@ -79,7 +79,7 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
 }
 
 #ifndef FOLD_CHUNK
-#define FOLD_CHUNK 16  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
+#define FOLD_CHUNK 64  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
 #endif
 
 // acc[base + i] += sc * (r[2i], r[2i+1]) for i < CH/2, as packed fp32x2 FMAs.
@@ -740,36 +740,43 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
       tc_fence_after();
       float s_row = 1.0f;
       if (!MX) s_row = row_ok ? __ldg(sa + (sa_per_row ? m : 0)) : 0.0f;
-#pragma unroll 1
+      // drain this thread's 128 accumulator columns into registers first and
+      // hand the accumulator back, so the next tile's MMAs overlap the stores
+      uint32_t r[4][32];
+      const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BN + half * 128);
+      tmem_ld_32x32b_x32(taddr, r[0]);
+      tmem_ld_32x32b_x32(taddr + 32, r[1]);
+      tmem_ld_32x32b_x32(taddr + 64, r[2]);
+      tmem_ld_32x32b_x32(taddr + 96, r[3]);
+      tmem_wait_ld_regs(r[0]);
+      tmem_wait_ld_regs(r[1]);
+      tmem_wait_ld_regs(r[2]);
+      tmem_wait_ld_regs(r[3]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[b]);
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(b * BN + half * 128 + 32 * c), r);
-        tmem_wait_ld();
-        if (c == 3) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&aempty[b]);
-        }
         const int nc = n0 + 32 * c;
         if (row_ok && nc < N) {
           float v[32];
           if (MX) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]);
           } else if (sb_per_col) {
             const float4 *sbv = reinterpret_cast<const float4 *>(sb + nc);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 q = (nc + 4 * i < N) ? __ldg(sbv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-              v[4 * i + 0] = __uint_as_float(r[4 * i + 0]) * (s_row * q.x);
-              v[4 * i + 1] = __uint_as_float(r[4 * i + 1]) * (s_row * q.y);
-              v[4 * i + 2] = __uint_as_float(r[4 * i + 2]) * (s_row * q.z);
-              v[4 * i + 3] = __uint_as_float(r[4 * i + 3]) * (s_row * q.w);
+              v[4 * i + 0] = __uint_as_float(r[c][4 * i + 0]) * (s_row * q.x);
+              v[4 * i + 1] = __uint_as_float(r[c][4 * i + 1]) * (s_row * q.y);
+              v[4 * i + 2] = __uint_as_float(r[c][4 * i + 2]) * (s_row * q.z);
+              v[4 * i + 3] = __uint_as_float(r[c][4 * i + 3]) * (s_row * q.w);
             }
           } else {
             const float s = s_row * __ldg(sb);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * s;
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]) * s;
           }
           store_row32(out + static_cast<int64_t>(m) * N + nc, v, N - nc);
         }
