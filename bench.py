@@ -107,6 +107,15 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
 
 
+def hold_gpu(cycles: int = 200_000):
+    """Keep the GPU busy (~0.1 ms spin) so that the launches recorded after this
+    are already queued when their start event runs: host launch latency stays
+    out of the per-kernel event times (the e2e measurement keeps it)."""
+    import torch
+
+    torch.cuda._sleep(cycles)
+
+
 # --------------------------------------------------------------------- ranks
 def max_over_ranks(x: float, device=None) -> float:
     """Max of a per-rank number over all ranks (identity with one process)."""
@@ -187,6 +196,7 @@ def run_gpu(args):
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush()
+            hold_gpu()
             e0, e1, e2 = ev[i]
             e0.record(stream)
             fb.quantize(xd, fb.E4M3, fb.TILE_1x128, q=qx, scales=sx)
@@ -268,6 +278,7 @@ def run_gpu(args):
             "data": "synthetic: seeded SplitMix64/Box-Muller N(0,1) X with 1% outlier channels x30, N(0,0.02) W",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": "replicas" if world > 1 else "1gpu",
                        "l2": "flushed between steps (256 MB write, outside the step events)",
+                       "host_latency": "a 0.1 ms GPU spin precedes each step's events, so launches are queued when timing starts",
                        "step_ms_quantize": round(sum(quant_ms) / len(quant_ms), 5),
                        "step_ms_gemm": round(gemm_avg, 5)},
             "roofline": {"bound": "tensor", "kernel": "gemm_fold_kernel", "achieved": round(achieved, 1),
@@ -300,6 +311,7 @@ def _time_kernel(fn, flush, stream, reps):
     ts = []
     for _ in range(reps):
         flush()
+        hold_gpu()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()

@@ -100,9 +100,19 @@ __device__ void drain_stages(uint64_t *full, int issued) {
 
 // Tile order: consecutive CTAs walk down M inside one N band so that a band
 // of W stays hot in L2 while X tiles are re-read.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int &mt, int &nt) {
-  nt = tile / num_m;
-  mt = tile - nt * num_m;
+// Tiles are taken in groups of `group_m` M-tiles: inside a group consecutive
+// tiles walk down M, then move to the next N band; the next group starts after
+// all N bands. A wave of CTAs therefore touches group_m X tiles (their rows stay
+// in L2 across the whole group) and a few W bands; the host sizes group_m so the
+// group's X rows take at most kRasterGroupBytes.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int &mt, int &nt) {
+  const int per_group = group_m * num_n;
+  const int g = tile / per_group;
+  const int local = tile - g * per_group;
+  const int first_m = g * group_m;
+  const int gm = min(group_m, num_m - first_m);
+  mt = first_m + local % gm;
+  nt = local / gm;
 }
 
 // =====================================================================
@@ -147,7 +157,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     gemm_fold_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
                      uint8_t *__restrict__ q_out, float *__restrict__ q_scales, int M, int N, int K, uint32_t idesc,
-                     int *dev_status) {
+                     int *dev_status, int group_m) {
   using C = FoldCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         int mt, nt;
-        tile_coords(tile, num_m, mt, nt);
+        tile_coords(tile, num_m, num_n, group_m, mt, nt);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     float2 acc[64];
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       int mt, nt;
-      tile_coords(tile, num_m, mt, nt);
+      tile_coords(tile, num_m, num_n, group_m, mt, nt);
       const int m = mt * BM + quarter * 32 + lane;
       const bool row_ok = m < M;
       const int nb = nt * (BN / 128) + half;
@@ -522,22 +532,17 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
+        // the whole BX-column partial in one load and one wait
+        uint32_t r[BX];
+        tmem_ld_chunk<BX>(taddr, r);
+        tmem_wait_ld_regs(r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
 #pragma unroll
-        for (int c = 0; c < BX / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + 16 * c, r);
-          tmem_wait_ld_regs(r);
-          if (c == BX / 16 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = 16 * c + i;
-            const float sx = __shfl_sync(0xffffffffu, x0[j / 32], j % 32);
-            acc[j] = fmaf(w0 * sx, __uint_as_float(r[i]), acc[j]);
-          }
+        for (int j = 0; j < BX; ++j) {
+          const float sx = __shfl_sync(0xffffffffu, x0[j / 32], j % 32);
+          acc[j] = fmaf(w0 * sx, __uint_as_float(r[j]), acc[j]);
         }
 #pragma unroll
         for (int r = 0; r < XR; ++r) {
@@ -593,7 +598,7 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
     gemm_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float *__restrict__ sa, int sa_per_row, const float *__restrict__ sb, int sb_per_col,
                      const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ out,
-                     int M, int N, int K, uint32_t idesc, int *dev_status) {
+                     int M, int N, int K, uint32_t idesc, int *dev_status, int group_m) {
   using C = AccCfg<MX, BN, STAGES, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -638,7 +643,7 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
       const int nblk128_b = (N + 127) / 128;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         int mt, nt;
-        tile_coords(tile, num_m, mt, nt);
+        tile_coords(tile, num_m, num_n, group_m, mt, nt);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tc) {
       int mt, nt;
-      tile_coords(tile, num_m, mt, nt);
+      tile_coords(tile, num_m, num_n, group_m, mt, nt);
       const int b = tc % NACC;
       const int m = mt * BM + quarter * 32 + lane;
       const bool row_ok = m < M;
@@ -815,6 +820,17 @@ bool ensure_smem(KernelT kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
 }
 
+// X rows a raster group may hold: well inside one die's half of the L2.
+constexpr int64_t kRasterGroupBytes = int64_t{32} << 20;
+
+int raster_group(int64_t M, int64_t K) {
+  const int64_t num_m = (M + BM - 1) / BM;
+  int64_t g = kRasterGroupBytes / (static_cast<int64_t>(BM) * (K > 0 ? K : 1));
+  if (g < 1) g = 1;
+  if (g > num_m) g = num_m;
+  return static_cast<int>(g);
+}
+
 int persistent_grid(int ntiles) {
   const int sms = device_sm_count();
   return ntiles < sms ? ntiles : sms;
@@ -857,7 +873,7 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
     const int ntiles = static_cast<int>(tiles256);
     kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
         ta, tb, sa, sb, out, q_out, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
+        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
   } else {
     constexpr int BN = 128, ST = 6;
     using C = FoldCfg<BN, ST>;
@@ -867,7 +883,7 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
     const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + 127) / 128));
     kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
         ta, tb, sa, sb, out, q_out, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
+        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
   }
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
@@ -907,7 +923,7 @@ fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
       ta, tb, sa, a_token ? 1 : 0, sb, b_token ? 1 : 0, nullptr, nullptr, out, static_cast<int>(M),
-      static_cast<int>(N), static_cast<int>(K), idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status);
+      static_cast<int>(N), static_cast<int>(K), idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -924,7 +940,7 @@ fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t 
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
       ta, tb, nullptr, 0, nullptr, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-      idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status);
+      idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status, raster_group(M, K));
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
