@@ -107,6 +107,23 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
 
 
+def make_l2_flush(dev):
+    """L2 flush between timed steps: write 256 MB (twice the L2), then read
+    another 256 MB so the write's dirty lines are written back before the next
+    timed kernel (otherwise an HBM-bound kernel pays for the flush's
+    write-back). Both run outside the timed events."""
+    import torch
+
+    wbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rbuf = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.zero_()
+        rbuf.sum()
+
+    return flush
+
+
 def hold_gpu(cycles: int = 200_000):
     """Keep the GPU busy (~0.1 ms spin) so that the launches recorded after this
     are already queued when their start event runs: host launch latency stays
@@ -163,10 +180,7 @@ def run_gpu(args):
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def flush():
-        flush_buf.zero_()
+    flush = make_l2_flush(dev)
 
     # ---- inputs (seeded, synthetic); weights quantized once, offline
     x_host = synth.prefill_x(M, K)
@@ -277,7 +291,7 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
             "data": "synthetic: seeded SplitMix64/Box-Muller N(0,1) X with 1% outlier channels x30, N(0,0.02) W",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": "replicas" if world > 1 else "1gpu",
-                       "l2": "flushed between steps (256 MB write, outside the step events)",
+                       "l2": "flushed between steps (256 MB write, then 256 MB read to clean it; outside the step events)",
                        "host_latency": "a 0.1 ms GPU spin precedes each step's events, so launches are queued when timing starts",
                        "step_ms_quantize": round(sum(quant_ms) / len(quant_ms), 5),
                        "step_ms_gemm": round(gemm_avg, 5)},
@@ -406,8 +420,7 @@ def run_workload(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks = measured_peaks()
-    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flush = flush_buf.zero_
+    flush = make_l2_flush(dev)
     if args.workload == "sweep":
         res = {"quantize_sweep_16384x8192": measure_sweep(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"])}
     elif args.workload == "decode":
