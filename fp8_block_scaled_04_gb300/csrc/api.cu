@@ -45,8 +45,8 @@ int device_sm_count() {
 
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
-bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
-                  uint32_t box_cols) {
+static bool make_tmap_2d(void *tmap_out, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base,
+                        uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows, uint32_t box_cols) {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -57,14 +57,23 @@ bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols
   });
   if (g_encode == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {ld};
+  cuuint64_t strides[1] = {ld * elem_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(static_cast<CUtensorMap *>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(static_cast<CUtensorMap *>(tmap_out), dtype, 2, const_cast<void *>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                  uint32_t box_cols) {
+  return make_tmap_2d(tmap_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, ld, box_rows, box_cols);
+}
+
+bool make_tmap_u16(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                   uint32_t box_cols) {
+  return make_tmap_2d(tmap_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, rows, cols, ld, box_rows, box_cols);
 }
 
 }  // namespace fp8bs

@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "fp8_math.cuh"
 #include "ptx.cuh"
@@ -77,6 +79,13 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
     }
   }
 }
+
+#ifndef FOLD_PAIR_STAGES
+#define FOLD_PAIR_STAGES 6  // 32 KB stages of the CTA-pair fold kernel
+#endif
+#ifndef FOLD_USE_PAIRS
+#define FOLD_USE_PAIRS 0  // 1: block-scaled GEMMs with M > 128 run on CTA pairs (measured slower)
+#endif
 
 #ifndef FOLD_CHUNK
 #define FOLD_CHUNK 64  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
@@ -131,7 +140,10 @@ struct FoldCfg {
   static constexpr int FIRST_CONSUMER_WARP = 4;
   static constexpr int THREADS = 32 * (FIRST_CONSUMER_WARP + CONSUMER_WARPS);
   static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  // output staging for the TMA-store epilogue: 32 KB, EPI_SLOTS 4 KB slots per fold warp
+  static constexpr int EPI_BYTES = 32768;
+  static constexpr int EPI_SLOTS = EPI_BYTES / (CONSUMER_WARPS * 4096);
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
   // setmaxnreg budgets. The increases are served from the registers the CTA
   // was launched with (registers per thread x THREADS), so the split must fit
   // in that pool or the increase never completes; launch_fold_tiles checks it
@@ -149,14 +161,88 @@ bool reg_split_fits(KernelT kernel, int threads, uint32_t needed) {
   return static_cast<uint64_t>(attr.numRegs) * static_cast<uint64_t>(threads) >= needed;
 }
 
+// Epilogue through shared memory and TMA stores. The warp's 32 rows x 128
+// columns leave as boxes 128 bytes wide and 32 rows high (bf16: two boxes of 64
+// columns; fp8 codes: one box of 128 columns), each written into one of the
+// warp's NSLOTS 4 KB staging slots in the 128-byte swizzled layout of the
+// output tensor map (16-byte chunk c of row r at chunk c ^ (r % 8)). Lane 0
+// issues the stores and returns at once; a slot is rewritten only after the
+// stores that read it have finished reading (bulk wait, read side). Rows past
+// M and columns past N lie outside the tensor map and are not written.
+template <int QFMT, int NSLOTS>
+__device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int row0, int n0, int M, int N,
+                                                  const CUtensorMap *tmo, uint8_t *slots, float *q_scales,
+                                                  int lane) {
+  const bool rows_in = row0 < M;
+  uint8_t *my_row = slots + lane * 128;
+  const int swz = lane & 7;
+  // the previous tile's stores from these slots have been read out
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  if constexpr (QFMT < 0) {
+    uint32_t p[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) p[i] = pack_bf16x2(acc[i].x, acc[i].y);
+#pragma unroll
+    for (int bx = 0; bx < 2; ++bx) {
+      uint8_t *row = my_row + (bx % NSLOTS) * 4096;
+      if (bx >= NSLOTS) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(row + ((c ^ swz) << 4)) =
+            make_uint4(p[32 * bx + 4 * c], p[32 * bx + 4 * c + 1], p[32 * bx + 4 * c + 2], p[32 * bx + 4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && rows_in && n0 + 64 * bx < N) {
+        tma_store_2d(tmo, slots + (bx % NSLOTS) * 4096, n0 + 64 * bx, row0);
+        bulk_commit_group();
+      }
+    }
+  } else {
+    // this thread's 128 columns are exactly one 1x128 group of the output row:
+    // round to bf16 (the unfused output), amax, scale, encode
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const uint32_t p = pack_bf16x2(acc[i].x, acc[i].y);
+      acc[i] = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
+      mx = max(mx, max(p & 0x7fffu, (p >> 16) & 0x7fffu));
+    }
+    float s, s_inv;
+    scale_pair(__uint_as_float(mx << 16), vmax_of(QFMT), s, s_inv);
+    if (m < M && n0 < N) q_scales[static_cast<int64_t>(n0 >> 7) * M + m] = s;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // 16 codes per chunk
+      float f[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        f[2 * i] = acc[8 * j + i].x;
+        f[2 * i + 1] = acc[8 * j + i].y;
+      }
+      const uint2 lo = encode8<QFMT>(reinterpret_cast<const float(&)[8]>(f[0]), s_inv);
+      const uint2 hi = encode8<QFMT>(reinterpret_cast<const float(&)[8]>(f[8]), s_inv);
+      *reinterpret_cast<uint4 *>(my_row + ((j ^ swz) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && rows_in && n0 < N) {
+      tma_store_2d(tmo, slots, n0, row0);
+      bulk_commit_group();
+    }
+  }
+}
+
 // QFMT < 0: bf16 output. QFMT = FP8_E4M3 / FP8_E5M2: the epilogue quantizes
 // its own bf16-rounded output with 1x128 scales (the next layer's activation
 // format) and writes codes + scales instead of bf16.
 template <int BN, int STAGES, int QFMT>
 __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     gemm_fold_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
-                     uint8_t *__restrict__ q_out, float *__restrict__ q_scales, int M, int N, int K, uint32_t idesc,
+                     const __grid_constant__ CUtensorMap tmO, const float *__restrict__ sa,
+                     const float *__restrict__ sb, float *__restrict__ q_scales, int M, int N, int K, uint32_t idesc,
                      int *dev_status, int group_m) {
   using C = FoldCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -186,6 +272,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
@@ -328,51 +415,12 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
         sb1 = sb2;
       }
       if (!ok) break;
-      // epilogue, straight from registers
-      if (row_ok) {
-        const int n0 = nb * 128;
-        if constexpr (QFMT < 0) {
-          uint16_t *dst = out + static_cast<int64_t>(m) * N + n0;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {  // 8 columns (16 bytes of bf16) per store
-            if (8 * j < N - n0) {
-              const uint4 w =
-                  make_uint4(pack_bf16x2(acc[4 * j].x, acc[4 * j].y), pack_bf16x2(acc[4 * j + 1].x, acc[4 * j + 1].y),
-                             pack_bf16x2(acc[4 * j + 2].x, acc[4 * j + 2].y),
-                             pack_bf16x2(acc[4 * j + 3].x, acc[4 * j + 3].y));
-              *reinterpret_cast<uint4 *>(dst + 8 * j) = w;
-            }
-          }
-        } else if (n0 < N) {
-          // this thread's 128 columns are exactly one 1x128 group of the output row:
-          // round to bf16 (the unfused output), amax, scale, encode
-          uint32_t mx = 0;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const uint32_t p = pack_bf16x2(acc[i].x, acc[i].y);
-            acc[i] = make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
-            mx = max(mx, max(p & 0x7fffu, (p >> 16) & 0x7fffu));
-          }
-          float s, s_inv;
-          scale_pair(__uint_as_float(mx << 16), vmax_of(QFMT), s, s_inv);
-          q_scales[static_cast<int64_t>(n0 >> 7) * M + m] = s;
-          uint8_t *qdst = q_out + static_cast<int64_t>(m) * N + n0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {  // 16 codes per store
-            float f[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              f[2 * i] = acc[8 * j + i].x;
-              f[2 * i + 1] = acc[8 * j + i].y;
-            }
-            const uint2 lo = encode8<QFMT>(reinterpret_cast<const float(&)[8]>(f[0]), s_inv);
-            const uint2 hi = encode8<QFMT>(reinterpret_cast<const float(&)[8]>(f[8]), s_inv);
-            *reinterpret_cast<uint4 *>(qdst + 16 * j) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-          }
-        }
-      }
+      fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * BM + quarter * 32, nb * 128, M, N, &tmO,
+                                            smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
+                                            lane);
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
   }
 
   tc_fence_before();
@@ -380,6 +428,223 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// =====================================================================
+// Fold kernel on CTA pairs (cta_group::2): 256 x 256 output tiles
+// =====================================================================
+// A cluster of two CTAs computes one 256 x 256 tile. Each CTA loads its own
+// 128 rows of X and its 128 rows of W (the pair MMA takes A rows and B columns
+// half from each CTA's shared memory, at the same offsets) and holds its 128
+// output rows x 256 columns in its own tensor memory. The even CTA issues the
+// pair MMAs; both CTAs' copies complete on its stage barriers, its commits
+// arrive on both CTAs' barriers, and both CTAs' fold warps hand partial
+// buffers back to it. A stage is 32 KB per CTA instead of 48 KB (6 stages fit,
+// more copies in flight) and each W tile is fetched once per pair.
+template <int STAGES>
+struct FoldPairCfg {
+  static constexpr int A_BYTES = BM * BK;   // this CTA's 128 rows of X
+  static constexpr int B_BYTES = 128 * BK;  // this CTA's 128 rows of W
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TM = 256, TN = 256;  // pair tile
+  static constexpr int CONSUMER_WARPS = 8;  // per CTA: 4 lane quarters x 2 column halves
+  static constexpr int FIRST_CONSUMER_WARP = 4;
+  static constexpr int THREADS = 32 * (FIRST_CONSUMER_WARP + CONSUMER_WARPS);
+  static constexpr uint32_t TMEM_COLS = 512;  // two partial buffers of 256 columns
+  // output staging of the TMA-store epilogue (one 4 KB slot per fold warp); it
+  // follows the last stage, so even a read of all 256 W rows from one CTA's
+  // last stage would stay inside the allocation
+  static constexpr int EPI_BYTES = 32768;
+  static constexpr int EPI_SLOTS = EPI_BYTES / (CONSUMER_WARPS * 4096);
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
+  static constexpr uint32_t REGS_CONTROL = 40;
+  static constexpr uint32_t REGS_FOLD = 224;
+  static constexpr uint32_t REGS_NEEDED = REGS_CONTROL * 32 * FIRST_CONSUMER_WARP + REGS_FOLD * 32 * CONSUMER_WARPS;
+};
+
+template <int STAGES, int QFMT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>::THREADS, 1)
+    gemm_fold_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmO, const float *__restrict__ sa,
+                          const float *__restrict__ sb, float *__restrict__ q_scales, int M, int N, int K,
+                          uint32_t idesc, int *dev_status, int group_m) {
+  using C = FoldPairCfg<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  __shared__ SharedCtl ctl;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int KB = K / BK;
+  const int num_m = (M + C::TM - 1) / C::TM;
+  const int num_n = (N + C::TN - 1) / C::TN;
+  const int ntiles = num_m * num_n;
+  const int nblk128 = (N + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * C::CONSUMER_WARPS);  // both CTAs' fold warps release to the even CTA
+    }
+    mbar_init(&drain, 1);
+    ctl.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&ctl.tmem_base, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const uint32_t full_lead = cluster_addr(&full[0], 0);      // stage s at + 8 s
+  const uint32_t tempty_lead = cluster_addr(&tempty[0], 0);  // buffer b at + 8 b
+
+  if (warp < C::FIRST_CONSUMER_WARP) {
+    regs_dealloc<C::REGS_CONTROL>();
+    if (warp == 0 && lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair; tile < ntiles && ok; tile += npairs) {
+        int mt, nt;
+        tile_coords(tile, num_m, num_n, group_m, mt, nt);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t *a_s = smem + s * C::STAGE_BYTES;
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+          const uint32_t bar = full_lead + 8u * static_cast<uint32_t>(s);
+          tma_load_2d_pair(a_s, &tmA, kb * BK, mt * C::TM + static_cast<int>(rank) * 128, bar);
+          tma_load_2d_pair(a_s + C::A_BYTES, &tmB, kb * BK, nt * C::TN + static_cast<int>(rank) * 128, bar);
+        }
+      }
+      if (!ok) {
+        flag_abort(&ctl, dev_status);
+        if (leader) {
+          drain_stages<STAGES>(full, it);
+        } else {
+          // this CTA's copies complete on the even CTA's barriers; give them time to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        }
+      }
+    } else if (warp == 1 && lane == 0 && leader) {
+      int it = 0, kc = 0;
+      bool ok = true;
+      for (int tile = pair; tile < ntiles && ok; tile += npairs) {
+        for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+          const int b = kc & 1;
+          const int s = it % STAGES;
+          if (!mbar_wait(&tempty[b], ((kc >> 1) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
+              !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::A_BYTES;
+          const uint32_t d = tmem + static_cast<uint32_t>(b * C::TN);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8f6f4_pair(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+          tc_commit_pair_mc(&empty[s], 0x3);
+          tc_commit_pair_mc(&tfull[b], 0x3);
+        }
+      }
+      if (!ok) flag_abort(&ctl, dev_status);
+      tc_commit_pair(&drain);
+      mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
+    }
+  } else {
+    regs_alloc<C::REGS_FOLD>();
+    const int cw = warp - C::FIRST_CONSUMER_WARP;
+    const int quarter = warp & 3;
+    const int half = cw >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int kc = 0;
+    bool ok = true;
+    float2 acc[64];
+    for (int tile = pair; tile < ntiles && ok; tile += npairs) {
+      int mt, nt;
+      tile_coords(tile, num_m, num_n, group_m, mt, nt);
+      const int m = mt * C::TM + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+      const bool row_ok = m < M;
+      const int nb = nt * 2 + half;
+      const bool col_ok = nb < nblk128;
+      const float *sa_row = sa + m;
+      const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+      float sa0 = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb0 = col_ok ? __ldg(sb_blk) : 0.0f;
+      float sa1 = (row_ok && KB > 1) ? __ldg(sa_row + static_cast<int64_t>(M)) : 0.0f;
+      float sb1 = (col_ok && KB > 1) ? __ldg(sb_blk + 1) : 0.0f;
+      for (int kb = 0; kb < KB; ++kb, ++kc) {
+        const int b = kc & 1;
+        const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
+        const float sb2 = (col_ok && kb + 2 < KB) ? __ldg(sb_blk + kb + 2) : 0.0f;
+        const bool got = mbar_wait(&tfull[b], (kc >> 1) & 1, kWaitTimeoutNs, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sc = sa0 * sb0;
+        const float2 sc2 = make_float2(sc, sc);
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * C::TN + half * 128);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t rb[64];
+          tmem_ld_32x32b_x64(taddr + 64 * c, rb);
+          tmem_wait_ld_regs(rb);
+          if (c == 1) {
+            // both loads of this buffer have landed: release it to the even CTA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * static_cast<uint32_t>(b));
+          }
+          fold_chunk<64>(acc, c * 32, sc2, rb);
+        }
+        sa0 = sa1;
+        sb0 = sb1;
+        sa1 = sa2;
+        sb1 = sb2;
+      }
+      if (!ok) break;
+      fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * C::TM + static_cast<int>(rank) * 128 + quarter * 32,
+                                            nb * 128, M, N, &tmO,
+                                            smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
+                                            lane);
+    }
+    if (!ok && lane == 0) flag_abort(&ctl, dev_status);
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's MMAs and both CTAs' tensor-memory reads are done
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
   }
 }
 
@@ -855,6 +1120,36 @@ fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *
 }
 
 template <int QFMT>
+fp8_status_t launch_fold_pairs(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+                               int b_fmt, uint16_t *out, uint8_t *q_out, float *q_scales, int64_t M, int64_t N,
+                               int64_t K, int *dev_status, cudaStream_t stream) {
+  constexpr int ST = FOLD_PAIR_STAGES;
+  using C = FoldPairCfg<ST>;
+  CUtensorMap ta, tb, to;
+  if (!make_tmap_u8(&ta, a, M, K, K, 128, BK) || !make_tmap_u8(&tb, b, N, K, K, 128, BK)) return FP8_ERR_CUDA;
+  if (QFMT < 0 ? !make_tmap_u16(&to, out, M, N, N, 32, 64) : !make_tmap_u8(&to, q_out, M, N, N, 32, 128))
+    return FP8_ERR_CUDA;
+  auto kern = gemm_fold_pair_kernel<ST, QFMT>;
+  if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
+  const int64_t ntiles = ((M + C::TM - 1) / C::TM) * ((N + C::TN - 1) / C::TN);
+  const int64_t pairs = std::min<int64_t>(ntiles, device_sm_count() / 2);
+  // raster groups in units of 256-row pair tiles
+  int64_t g = kRasterGroupBytes / (static_cast<int64_t>(C::TM) * K);
+  g = std::max<int64_t>(1, std::min<int64_t>(g, (M + C::TM - 1) / C::TM));
+  kern<<<static_cast<unsigned>(2 * pairs), C::THREADS, C::SMEM, stream>>>(
+      ta, tb, to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+      idesc_f8f6f4(a_fmt, b_fmt, 256, 256), dev_status, static_cast<int>(g));
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// CTA pairs need at least 256 rows and enough pair tiles to fill the GPU.
+bool use_pairs(int64_t M, int64_t N) {
+  const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  return FOLD_USE_PAIRS && M > 128 && 2 * pair_tiles >= device_sm_count();
+}
+
+template <int QFMT>
 fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                                int b_fmt, uint16_t *out, uint8_t *q_out, float *q_scales, int64_t M, int64_t N,
                                int64_t K, int *dev_status, cudaStream_t stream) {
@@ -862,8 +1157,11 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
   const int sms = device_sm_count();
   const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
   const bool wide = tiles256 >= sms;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK)) return FP8_ERR_CUDA;
+  // output boxes: 32 rows x 128 bytes (bf16: 64 columns; fp8 codes: 128)
+  if (QFMT < 0 ? !make_tmap_u16(&to, out, M, N, N, 32, 64) : !make_tmap_u8(&to, q_out, M, N, N, 32, 128))
+    return FP8_ERR_CUDA;
   if (wide) {
     constexpr int BN = 256, ST = 4;
     using C = FoldCfg<BN, ST>;
@@ -872,7 +1170,7 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
     if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
     const int ntiles = static_cast<int>(tiles256);
     kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-        ta, tb, sa, sb, out, q_out, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        ta, tb, to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
   } else {
     constexpr int BN = 128, ST = 6;
@@ -882,7 +1180,7 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
     if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
     const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + 127) / 128));
     kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-        ta, tb, sa, sb, out, q_out, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        ta, tb, to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
   }
   note_launches(1);
@@ -898,12 +1196,21 @@ fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *
   if (M <= 16) return launch_fold_swap<16, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
   if (M <= 32) return launch_fold_swap<32, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
   if (M <= 64) return launch_fold_swap<64, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
+  if (use_pairs(M, N))
+    return launch_fold_pairs<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
   return launch_fold_tiles<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
 }
 
 fp8_status_t launch_gemm_fold_quantized(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
                                         int a_fmt, int b_fmt, int out_fmt, uint8_t *q_out, float *q_scales,
                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {
+  if (use_pairs(M, N)) {
+    if (out_fmt == FP8_E4M3)
+      return launch_fold_pairs<FP8_E4M3>(a, sa, b, sb, a_fmt, b_fmt, nullptr, q_out, q_scales, M, N, K, dev_status,
+                                         stream);
+    return launch_fold_pairs<FP8_E5M2>(a, sa, b, sb, a_fmt, b_fmt, nullptr, q_out, q_scales, M, N, K, dev_status,
+                                       stream);
+  }
   if (out_fmt == FP8_E4M3)
     return launch_fold_tiles<FP8_E4M3>(a, sa, b, sb, a_fmt, b_fmt, nullptr, q_out, q_scales, M, N, K, dev_status,
                                        stream);

@@ -66,5 +66,9 @@ fp8_status_t launch_wait_probe(int *dev_status, uint64_t timeout_ns, cudaStream_
 // row stride ld bytes), box = box_cols x box_rows, 128-byte swizzle.
 bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
                   uint32_t box_cols);
+// The same over a row-major 16-bit matrix (bf16 output): ld in elements; the
+// box's inner extent box_cols x 2 bytes must be at most 128 bytes.
+bool make_tmap_u16(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                   uint32_t box_cols);
 
 }  // namespace fp8bs

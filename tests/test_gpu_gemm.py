@@ -62,6 +62,19 @@ def test_fold_ragged_shapes(M, N, K):
     assert bad == 0, (bad, worst)
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 256), (2000, 2480, 384), (4096, 2432, 640)])
+def test_fold_on_cta_pairs(M, N, K):
+    """Shapes with enough 256 x 256 tiles for the CTA-pair kernel (ragged in M and N)."""
+    x = synth.bf16_matrix(M, K, 1.0, 60 + M, 61 + K, 0.01, 50.0)
+    w = synth.bf16_matrix(N, K, 0.02, 62 + N)
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), np.arange(M - 130, M), np.arange(120, 390)]))
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, rows=rows)
+    bad, worst = within_tolerance(out_f64(out)[rows], ref, bound)
+    assert bad == 0, (bad, worst)
+
+
 def test_fold_small_integers_exact():
     """Integer-valued FP8 operands, power-of-two scales, K <= 512: fp32 sums are exact."""
     rng = np.random.default_rng(1)
