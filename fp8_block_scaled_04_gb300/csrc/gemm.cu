@@ -247,7 +247,12 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
   using C = FoldCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  // One commit per k-block: empty[s] completes when the MMAs of the k-block in
+  // stage s are done, which frees the stage for the producer and tells the fold
+  // warps that the partial of that k-block is in tensor memory. The fold warps
+  // can wait on it by parity because the stage's next k-block (kc + STAGES)
+  // cannot complete before they release its buffer after k-block kc + 2.
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[2], drain;
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -263,10 +268,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], C::CONSUMER_WARPS);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&tempty[b], C::CONSUMER_WARPS);
     mbar_init(&drain, 1);
     ctl.abort = 0;
     fence_barrier_init();
@@ -327,7 +329,6 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
           for (int k = 0; k < BK / 32; ++k)
             mma_f8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, k > 0 ? 1u : 0u);
           tc_commit(&empty[s]);
-          tc_commit(&tfull[b]);
         }
       }
       if (!ok) flag_abort(&ctl, dev_status);
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
         const int b = kc & 1;
         const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
         const float sb2 = (col_ok && kb + 2 < KB) ? __ldg(sb_blk + kb + 2) : 0.0f;
-        const bool got = mbar_wait(&tfull[b], (kc >> 1) & 1, kWaitTimeoutNs, &ctl.abort);
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -472,7 +473,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
   using C = FoldPairCfg<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  // one commit per k-block (multicast to both CTAs' empty[s]), as in the
+  // single-CTA kernel: the fold warps wait on the stage barrier
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[2], drain;
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -492,10 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * C::CONSUMER_WARPS);  // both CTAs' fold warps release to the even CTA
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&tempty[b], 2 * C::CONSUMER_WARPS);  // both CTAs' fold warps release to the even CTA
     mbar_init(&drain, 1);
     ctl.abort = 0;
     fence_barrier_init();
@@ -567,7 +567,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
           for (int k = 0; k < BK / 32; ++k)
             mma_f8f6f4_pair(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, k > 0 ? 1u : 0u);
           tc_commit_pair_mc(&empty[s], 0x3);
-          tc_commit_pair_mc(&tfull[b], 0x3);
         }
       }
       if (!ok) flag_abort(&ctl, dev_status);
@@ -602,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
         const int b = kc & 1;
         const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
         const float sb2 = (col_ok && kb + 2 < KB) ? __ldg(sb_blk + kb + 2) : 0.0f;
-        const bool got = mbar_wait(&tfull[b], (kc >> 1) & 1, kWaitTimeoutNs, &ctl.abort);
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -675,7 +674,11 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   using C = SwapCfg<BX, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[C::NBUF], tempty[C::NBUF], drain;
+  // one commit per k-block; the fold warps wait on the stage barrier (the
+  // stage's next k-block needs the release of k-block kc + NBUF first, and
+  // STAGES > NBUF)
+  static_assert(STAGES > C::NBUF, "stage barrier parity");
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[C::NBUF], drain;
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -690,10 +693,7 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < C::NBUF; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
-    }
+    for (int b = 0; b < C::NBUF; ++b) mbar_init(&tempty[b], 4);
     mbar_init(&drain, 1);
     ctl.abort = 0;
     fence_barrier_init();
@@ -753,7 +753,6 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
           for (int k = 0; k < BK / 32; ++k)
             mma_f8f6f4(d, sdesc_k_sw128(w0 + 32 * k), sdesc_k_sw128(x0 + 32 * k), idesc, k > 0 ? 1u : 0u);
           tc_commit(&empty[s]);
-          tc_commit(&tfull[b]);
         }
       }
       if (!ok) flag_abort(&ctl, dev_status);
@@ -790,7 +789,7 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         const int b = kc % C::NBUF;
         load_sx(kb + 2, x2);
         const float w2 = kb + 2 < KB ? __ldg(sb_blk + kb + 2) : 0.0f;
-        const bool got = mbar_wait(&tfull[b], (kc / C::NBUF) & 1, kWaitTimeoutNs, &ctl.abort);
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
