@@ -61,10 +61,12 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
+// Two fp32 -> bf16 round-to-nearest-even conversions in one instruction
+// (cvt.rn.bf16x2.f32); lo lands in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return a | (b << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Store 32 fp32 values (one row, 32 consecutive columns) as bf16; n_left is
@@ -82,6 +84,9 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
 
 #ifndef FOLD_PAIR_STAGES
 #define FOLD_PAIR_STAGES 6  // 32 KB stages of the CTA-pair fold kernel
+#endif
+#ifndef FOLD_WIDE_STAGES
+#define FOLD_WIDE_STAGES 4  // stages of the 128 x 256 fold kernel (3 leaves room for two epilogue slots per warp)
 #endif
 #ifndef FOLD_USE_PAIRS
 #define FOLD_USE_PAIRS 0  // 1: block-scaled GEMMs with M > 128 run on CTA pairs (measured slower)
@@ -140,10 +145,14 @@ struct FoldCfg {
   static constexpr int FIRST_CONSUMER_WARP = 4;
   static constexpr int THREADS = 32 * (FIRST_CONSUMER_WARP + CONSUMER_WARPS);
   static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  // output staging for the TMA-store epilogue: 32 KB, EPI_SLOTS 4 KB slots per fold warp
-  static constexpr int EPI_BYTES = 32768;
-  static constexpr int EPI_SLOTS = EPI_BYTES / (CONSUMER_WARPS * 4096);
+  // output staging for the TMA-store epilogue: EPI_SLOTS 4 KB slots per fold
+  // warp (two make the epilogue wait-free), as many as the shared memory left
+  // by the stages holds
+  static constexpr int SMEM_LIMIT = 232448 - 1024 - 512;  // opt-in maximum - alignment - static barriers
+  static constexpr int EPI_SLOTS = (SMEM_LIMIT - STAGES * STAGE_BYTES) / (CONSUMER_WARPS * 4096) >= 2 ? 2 : 1;
+  static constexpr int EPI_BYTES = EPI_SLOTS * CONSUMER_WARPS * 4096;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
+  static_assert(SMEM + 512 <= 232448, "shared memory budget");
   // setmaxnreg budgets. The increases are served from the registers the CTA
   // was launched with (registers per thread x THREADS), so the split must fit
   // in that pool or the increase never completes; launch_fold_tiles checks it
@@ -456,9 +465,11 @@ struct FoldPairCfg {
   // output staging of the TMA-store epilogue (one 4 KB slot per fold warp); it
   // follows the last stage, so even a read of all 256 W rows from one CTA's
   // last stage would stay inside the allocation
-  static constexpr int EPI_BYTES = 32768;
-  static constexpr int EPI_SLOTS = EPI_BYTES / (CONSUMER_WARPS * 4096);
+  static constexpr int SMEM_LIMIT = 232448 - 1024 - 512;
+  static constexpr int EPI_SLOTS = (SMEM_LIMIT - STAGES * STAGE_BYTES) / (CONSUMER_WARPS * 4096) >= 2 ? 2 : 1;
+  static constexpr int EPI_BYTES = EPI_SLOTS * CONSUMER_WARPS * 4096;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
+  static_assert(SMEM + 512 <= 232448, "shared memory budget");
   static constexpr uint32_t REGS_CONTROL = 40;
   static constexpr uint32_t REGS_FOLD = 224;
   static constexpr uint32_t REGS_NEEDED = REGS_CONTROL * 32 * FIRST_CONSUMER_WARP + REGS_FOLD * 32 * CONSUMER_WARPS;
@@ -1162,7 +1173,7 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
   if (QFMT < 0 ? !make_tmap_u16(&to, out, M, N, N, 32, 64) : !make_tmap_u8(&to, q_out, M, N, N, 32, 128))
     return FP8_ERR_CUDA;
   if (wide) {
-    constexpr int BN = 256, ST = 4;
+    constexpr int BN = 256, ST = FOLD_WIDE_STAGES;
     using C = FoldCfg<BN, ST>;
     if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
     auto kern = gemm_fold_kernel<BN, ST, QFMT>;
