@@ -178,10 +178,13 @@ bool reg_split_fits(KernelT kernel, int threads, uint32_t needed) {
 // issues the stores and returns at once; a slot is rewritten only after the
 // stores that read it have finished reading (bulk wait, read side). Rows past
 // M and columns past N lie outside the tensor map and are not written.
-template <int QFMT, int NSLOTS>
+// mid() runs once the first store is issued, while that store reads shared
+// memory (the caller issues the next tile's first scale loads there, so their
+// latency hides behind the rest of the epilogue).
+template <int QFMT, int NSLOTS, typename Mid>
 __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int row0, int n0, int M, int N,
                                                   const CUtensorMap *tmo, uint8_t *slots, float *q_scales,
-                                                  int lane) {
+                                                  int lane, Mid &&mid) {
   const bool rows_in = row0 < M;
   uint8_t *my_row = slots + lane * 128;
   const int swz = lane & 7;
@@ -209,6 +212,7 @@ __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int 
         tma_store_2d(tmo, slots + (bx % NSLOTS) * 4096, n0 + 64 * bx, row0);
         bulk_commit_group();
       }
+      if (bx == 0) mid();
     }
   } else {
     // this thread's 128 columns are exactly one 1x128 group of the output row:
@@ -241,6 +245,7 @@ __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int 
       tma_store_2d(tmo, slots, n0, row0);
       bulk_commit_group();
     }
+    mid();
   }
 }
 
@@ -354,6 +359,22 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     int kc = 0;
     bool ok = true;
     float2 acc[64];
+    // first two scale pairs of a tile: loaded in the previous tile's epilogue
+    // (see fold_epilogue_tma), else at the top of the tile
+    auto first_scales = [&](int t, float &a0, float &b0, float &a1, float &b1) {
+      int tm, tn;
+      tile_coords(t, num_m, num_n, group_m, tm, tn);
+      const int tr = tm * BM + quarter * 32 + lane;
+      const int tb = tn * (BN / 128) + half;
+      const float *pa = sa + tr;
+      const float *pb = sb + static_cast<int64_t>(tb) * KB;
+      a0 = tr < M ? __ldg(pa) : 0.0f;
+      b0 = tb < nblk128 ? __ldg(pb) : 0.0f;
+      a1 = (tr < M && KB > 1) ? __ldg(pa + static_cast<int64_t>(M)) : 0.0f;
+      b1 = (tb < nblk128 && KB > 1) ? __ldg(pb + 1) : 0.0f;
+    };
+    float nsa0 = 0.0f, nsb0 = 0.0f, nsa1 = 0.0f, nsb1 = 0.0f;
+    bool have_next = false;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, num_m, num_n, group_m, mt, nt);
@@ -366,10 +387,15 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
       // scale prefetch, two chunks ahead
-      float sa0 = row_ok ? __ldg(sa_row) : 0.0f;
-      float sb0 = col_ok ? __ldg(sb_blk) : 0.0f;
-      float sa1 = (row_ok && KB > 1) ? __ldg(sa_row + static_cast<int64_t>(M)) : 0.0f;
-      float sb1 = (col_ok && KB > 1) ? __ldg(sb_blk + 1) : 0.0f;
+      float sa0, sb0, sa1, sb1;
+      if (have_next) {
+        sa0 = nsa0;
+        sb0 = nsb0;
+        sa1 = nsa1;
+        sb1 = nsb1;
+      } else {
+        first_scales(tile, sa0, sb0, sa1, sb1);
+      }
       for (int kb = 0; kb < KB; ++kb, ++kc) {
         const int b = kc & 1;
         const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
@@ -425,9 +451,13 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
         sb1 = sb2;
       }
       if (!ok) break;
+      const int next = tile + static_cast<int>(gridDim.x);
       fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * BM + quarter * 32, nb * 128, M, N, &tmO,
                                             smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
-                                            lane);
+                                            lane, [&]() {
+                                              have_next = next < ntiles;
+                                              if (have_next) first_scales(next, nsa0, nsb0, nsa1, nsb1);
+                                            });
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
     if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
@@ -593,6 +623,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
     int kc = 0;
     bool ok = true;
     float2 acc[64];
+    // first two scale pairs of a tile, as in the single-CTA kernel
+    auto first_scales = [&](int t, float &a0, float &b0, float &a1, float &b1) {
+      int tm, tn;
+      tile_coords(t, num_m, num_n, group_m, tm, tn);
+      const int tr = tm * C::TM + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+      const int tb = tn * 2 + half;
+      const float *pa = sa + tr;
+      const float *pb = sb + static_cast<int64_t>(tb) * KB;
+      a0 = tr < M ? __ldg(pa) : 0.0f;
+      b0 = tb < nblk128 ? __ldg(pb) : 0.0f;
+      a1 = (tr < M && KB > 1) ? __ldg(pa + static_cast<int64_t>(M)) : 0.0f;
+      b1 = (tb < nblk128 && KB > 1) ? __ldg(pb + 1) : 0.0f;
+    };
+    float nsa0 = 0.0f, nsb0 = 0.0f, nsa1 = 0.0f, nsb1 = 0.0f;
+    bool have_next = false;
     for (int tile = pair; tile < ntiles && ok; tile += npairs) {
       int mt, nt;
       tile_coords(tile, num_m, num_n, group_m, mt, nt);
@@ -604,10 +649,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
       const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      float sa0 = row_ok ? __ldg(sa_row) : 0.0f;
-      float sb0 = col_ok ? __ldg(sb_blk) : 0.0f;
-      float sa1 = (row_ok && KB > 1) ? __ldg(sa_row + static_cast<int64_t>(M)) : 0.0f;
-      float sb1 = (col_ok && KB > 1) ? __ldg(sb_blk + 1) : 0.0f;
+      float sa0, sb0, sa1, sb1;
+      if (have_next) {
+        sa0 = nsa0;
+        sb0 = nsb0;
+        sa1 = nsa1;
+        sb1 = nsb1;
+      } else {
+        first_scales(tile, sa0, sb0, sa1, sb1);
+      }
       for (int kb = 0; kb < KB; ++kb, ++kc) {
         const int b = kc & 1;
         const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
@@ -640,10 +690,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
         sb1 = sb2;
       }
       if (!ok) break;
+      const int next = tile + npairs;
       fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * C::TM + static_cast<int>(rank) * 128 + quarter * 32,
                                             nb * 128, M, N, &tmO,
                                             smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
-                                            lane);
+                                            lane, [&]() {
+                                              have_next = next < ntiles;
+                                              if (have_next) first_scales(next, nsa0, nsb0, nsa1, nsb1);
+                                            });
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
     if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
