@@ -901,6 +901,237 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   }
 }
 
+
+// Split-K variant of the decode kernel, for too few 128-row W blocks to occupy
+// the GPU: each tile's K range is split over the S CTAs of a cluster (launch
+// attribute). Every CTA folds its share of the k-blocks; the non-leading CTAs
+// leave their fp32 partials in their own shared memory and signal the leader
+// (rank 0), which adds them in rank order (a fixed order: the result does not
+// depend on timing) through distributed shared memory, writes the output and
+// lets them go. A separate kernel: folding the split into the unsplit kernel
+// made its launches ~2 us slower (measured).
+template <int BX, int STAGES>
+struct SwapSplitCfg {
+  static constexpr int W_BYTES = BM * BK;
+  static constexpr int X_BYTES = BX * BK;
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+  static constexpr int NBUF = 4;                       // tensor-memory partial buffers
+  static constexpr int THREADS = 32 * (2 + 4);
+  static constexpr uint32_t TMEM_COLS = NBUF * BX <= 32 ? 32 : (NBUF * BX <= 64 ? 64 : (NBUF * BX <= 128 ? 128 : 256));
+  static constexpr int RED_BYTES = BM * BX * 4;  // this CTA's partial, [BX][128] fp32
+  static constexpr int SMEM = STAGES * STAGE_BYTES + RED_BYTES + 1024;
+  static_assert(BX % 16 == 0 && BX <= 64, "MMA N side");
+  static_assert(SMEM + 256 <= 232448, "shared memory budget");
+};
+
+template <int BX, int STAGES>
+__global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
+    gemm_fold_swap_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                          const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
+                          int M, int N, int K, uint32_t idesc, int *dev_status) {
+  using C = SwapSplitCfg<BX, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  // one commit per k-block; the fold warps wait on the stage barrier (the
+  // stage's next k-block needs the release of k-block kc + NBUF first, and
+  // STAGES > NBUF)
+  static_assert(STAGES > C::NBUF, "stage barrier parity");
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[C::NBUF], drain, red_full, red_done;
+  __shared__ SharedCtl ctl;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = K / BK;
+  const int num_x = (M + BX - 1) / BX;
+  const int num_w = (N + BM - 1) / BM;
+  const int ntiles = num_x * num_w;
+  // cluster geometry and this CTA's k-blocks
+  const int S = static_cast<int>(cluster_nctarank());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int first_tile = static_cast<int>(blockIdx.x) / S;
+  const int tile_step = static_cast<int>(gridDim.x) / S;
+  const int kb_lo = rank * KB / S;
+  const int kb_hi = (rank + 1) * KB / S;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < C::NBUF; ++b) mbar_init(&tempty[b], 4);
+    mbar_init(&drain, 1);
+    mbar_init(&red_full, 4 * (S - 1));  // every fold warp of every other CTA
+    mbar_init(&red_done, 4);                        // the leader's fold warps
+    ctl.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every CTA's barriers exist before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = first_tile; tile < ntiles && ok; tile += tile_step) {
+        const int wt = tile / num_x, xt = tile - wt * num_x;
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t *w_s = smem + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(w_s, &tmW, kb * BK, wt * BM, &full[s]);
+          tma_load_2d(w_s + C::W_BYTES, &tmX, kb * BK, xt * BX, &full[s]);
+        }
+      }
+      if (!ok) {
+        flag_abort(&ctl, dev_status);
+        drain_stages<STAGES>(full, it);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, kc = 0;
+      bool ok = true;
+      for (int tile = first_tile; tile < ntiles && ok; tile += tile_step) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it, ++kc) {
+          const int b = kc % C::NBUF;
+          const int s = it % STAGES;
+          if (!mbar_wait(&tempty[b], ((kc / C::NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
+              !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t x0 = w0 + C::W_BYTES;
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8f6f4(d, sdesc_k_sw128(w0 + 32 * k), sdesc_k_sw128(x0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+      }
+      if (!ok) flag_abort(&ctl, dev_status);
+      tc_commit(&drain);
+      mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // this thread's W row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    constexpr int XR = (BX + 31) / 32;  // activation-scale registers per lane
+    float *red = reinterpret_cast<float *>(smem + STAGES * C::STAGE_BYTES);  // [BX][128]
+    int kc = 0, tn = 0;
+    bool ok = true;
+    float acc[BX];
+    for (int tile = first_tile; tile < ntiles && ok; tile += tile_step, ++tn) {
+      const int wt = tile / num_x, xt = tile - wt * num_x;
+      const int n = wt * BM + row;  // this thread's output column
+      const int m0 = xt * BX;
+      const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
+#pragma unroll
+      for (int j = 0; j < BX; ++j) acc[j] = 0.0f;
+      // lane l holds s_x[kb, m0 + 32 r + l]; prefetched two chunks ahead
+      float x0[XR], x1[XR], x2[XR];
+      auto load_sx = [&](int kbq, float (&dst)[XR]) {
+#pragma unroll
+        for (int r = 0; r < XR; ++r) {
+          const int mm = m0 + 32 * r + lane;
+          dst[r] = (kbq < kb_hi && 32 * r + lane < BX && mm < M) ? __ldg(sa + static_cast<int64_t>(kbq) * M + mm) : 0.0f;
+        }
+      };
+      load_sx(kb_lo, x0);
+      load_sx(kb_lo + 1, x1);
+      float w0 = __ldg(sb_blk + kb_lo), w1 = kb_lo + 1 < kb_hi ? __ldg(sb_blk + kb_lo + 1) : 0.0f;
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++kc) {
+        const int b = kc % C::NBUF;
+        load_sx(kb + 2, x2);
+        const float w2 = kb + 2 < kb_hi ? __ldg(sb_blk + kb + 2) : 0.0f;
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
+        // the whole BX-column partial in one load and one wait
+        uint32_t r[BX];
+        tmem_ld_chunk<BX>(taddr, r);
+        tmem_wait_ld_regs(r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+#pragma unroll
+        for (int j = 0; j < BX; ++j) {
+          const float sx = __shfl_sync(0xffffffffu, x0[j / 32], j % 32);
+          acc[j] = fmaf(w0 * sx, __uint_as_float(r[j]), acc[j]);
+        }
+#pragma unroll
+        for (int r = 0; r < XR; ++r) {
+          x0[r] = x1[r];
+          x1[r] = x2[r];
+        }
+        w0 = w1;
+        w1 = w2;
+      }
+      if (!ok) break;
+      {
+        const uint32_t phase = static_cast<uint32_t>(tn & 1);
+        if (rank != 0) {
+          // leave this CTA's partial for the leader and wait until it has been read
+#pragma unroll
+          for (int j = 0; j < BX; ++j) red[j * BM + row] = acc[j];
+          __syncwarp();
+          if (lane == 0) mbar_arrive_release_cluster(cluster_addr(&red_full, 0));
+          const bool done = mbar_wait(&red_done, phase, kWaitTimeoutNs, &ctl.abort);
+          if (!__all_sync(0xffffffffu, done)) ok = false;
+          continue;
+        }
+        const bool in = mbar_wait_acquire_cluster(&red_full, phase, kWaitTimeoutNs);
+        if (!__all_sync(0xffffffffu, in)) {
+          ok = false;
+          break;
+        }
+        for (int p = 1; p < S; ++p) {
+          const uint32_t base = cluster_addr(red, static_cast<uint32_t>(p)) + 4u * static_cast<uint32_t>(row);
+#pragma unroll
+          for (int j = 0; j < BX; ++j) acc[j] += ld_shared_cluster_f32(base + 4u * static_cast<uint32_t>(j * BM));
+        }
+        __syncwarp();
+        if (lane == 0)
+          for (int p = 1; p < S; ++p) mbar_arrive_release_cluster(cluster_addr(&red_done, static_cast<uint32_t>(p)));
+      }
+      if (n < N) {
+#pragma unroll
+        for (int j = 0; j < BX; ++j) {
+          const int m = m0 + j;
+          if (m < M) out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+        }
+      }
+    }
+    if (!ok && lane == 0) flag_abort(&ctl, dev_status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // =====================================================================
 // Tensor-memory accumulating kernel: epilogue-scaled (MX = false) or
 // block-scaled MXFP8 (MX = true)
@@ -1165,20 +1396,73 @@ int persistent_grid(int ntiles) {
   return ntiles < sms ? ntiles : sms;
 }
 
+// K splits for the decode kernel. Without a split, a tile is one 128-row W block
+// streamed over all of K by one CTA, and when there are fewer tiles than SMs the
+// idle SMs' share of HBM bandwidth is lost. With S splits the tile's K range is
+// spread over a cluster of S CTAs. S minimises the largest number of CTAs any SM
+// runs divided by S (the time one SM needs for its share, in units of a whole
+// tile), with all CTAs resident at once (units * S <= capacity), S <= 8 (portable
+// cluster size) and at least two k-blocks per CTA; ties go to the smaller S.
+int swap_split(int64_t units, int64_t KB, int sms, int capacity) {
+  if (units * 10 >= static_cast<int64_t>(sms) * 9) return 1;  // already fills the GPU
+  int best = 1;
+  double best_t = static_cast<double>((units + sms - 1) / sms);
+  for (int S = 2; S <= 8; ++S) {
+    if (2 * S > KB || units * S > capacity) break;
+    const double t = static_cast<double>((units * S + sms - 1) / sms) / S;
+    if (t < best_t - 1e-9) {
+      best = S;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
 template <int BX, int ST>
 fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
                               cudaStream_t stream) {
-  using C = SwapCfg<BX, ST>;
   CUtensorMap tx, tw;
   if (!make_tmap_u8(&tx, a, M, K, K, BX, BK) || !make_tmap_u8(&tw, b, N, K, K, BM, BK)) return FP8_ERR_CUDA;
-  auto kern = gemm_fold_swap_kernel<BX, ST>;
-  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + BX - 1) / BX) * ((N + BM - 1) / BM));
   // the MMA's A operand is W (format b_fmt), its B operand is X (a_fmt)
+  const uint32_t idesc = idesc_f8f6f4(b_fmt, a_fmt, BM, BX);
+  const int sms = device_sm_count();
+  if (ntiles * 10 < sms * 9 && K / BK >= 4) {
+    // split-K clusters; 5 stages (the fewest the stage-barrier parity allows)
+    // so that two CTAs fit on an SM where registers allow
+    constexpr int STS = 5;
+    using CS = SwapSplitCfg<BX, STS>;
+    auto kern = gemm_fold_swap_split_kernel<BX, STS>;
+    if (!ensure_smem(kern, CS::SMEM)) return FP8_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, CS::THREADS, CS::SMEM) != cudaSuccess) occ = 1;
+    const int S = swap_split(ntiles, K / BK, sms, std::max(occ, 1) * sms);
+    if (S > 1) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(ntiles * S), 1, 1);
+      cfg.blockDim = dim3(CS::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = CS::SMEM;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tx, tw, sa, sb, out, static_cast<int>(M),
+                                               static_cast<int>(N), static_cast<int>(K), idesc, dev_status);
+      note_launches(1);
+      return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+    }
+  }
+  using C = SwapCfg<BX, ST>;
+  auto kern = gemm_fold_swap_kernel<BX, ST>;
+  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(tx, tw, sa, sb, out, static_cast<int>(M),
-                                                                 static_cast<int>(N), static_cast<int>(K),
-                                                                 idesc_f8f6f4(b_fmt, a_fmt, BM, BX), dev_status);
+                                                                 static_cast<int>(N), static_cast<int>(K), idesc,
+                                                                 dev_status);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -1257,6 +1541,7 @@ fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
                               cudaStream_t stream) {
   // Few activation rows (decode): swap operands so the 128-row MMA side is W.
+  // 8-stage rings (5 to 12 stages measured the same or slower)
   if (M <= 16) return launch_fold_swap<16, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
   if (M <= 32) return launch_fold_swap<32, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
   if (M <= 64) return launch_fold_swap<64, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);

@@ -75,6 +75,36 @@ def test_fold_on_cta_pairs(M, N, K):
     assert bad == 0, (bad, worst)
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 7168, 16384), (32, 2048, 4096), (64, 4096, 1024), (16, 1040, 2048),
+                                   (5, 768, 896), (48, 3072, 7168)])
+def test_decode_split_k(M, N, K):
+    """Few 128-row weight blocks: the K range of each block is split over a CTA cluster
+    (ragged N edge, odd M, K ranges that do not divide evenly)."""
+    x = synth.bf16_matrix(M, K, 1.0, 70 + M, 71 + K, 0.01, 50.0)
+    w = synth.bf16_matrix(N, K, 0.02, 72 + N)
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    cols = np.unique(np.concatenate([np.arange(0, N, 7), np.arange(N - 140, N)]))
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, cols=cols)
+    bad, worst = within_tolerance(out_f64(out)[:, cols], ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+def test_decode_split_k_small_integers_exact():
+    """Split-K partial sums of integer-valued operands with power-of-two scales are exact."""
+    rng = np.random.default_rng(11)
+    M, N, K = 16, 1024, 512 * 8
+    a = oracle.encode(rng.integers(-4, 5, (M, K)).astype(np.float32), fb.E4M3)
+    b = oracle.encode(rng.integers(-4, 5, (N, K)).astype(np.float32), fb.E4M3)
+    # scales 2^-1..2^1: every partial is a multiple of 2^-2 below 2^18, so fp32 sums are exact
+    sa = (2.0 ** rng.integers(-1, 2, (K // 128) * M)).astype(np.float32)
+    sb = (2.0 ** rng.integers(-1, 2, ((N + 127) // 128) * (K // 128))).astype(np.float32)
+    out = _run_blockscaled(a, sa, fb.TILE_1x128, b, sb, fb.BLOCK_128x128)
+    ref, _ = oracle.gemm(a, sa, fb.TILE_1x128, b, sb, fb.BLOCK_128x128)
+    expect = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(out_f64(out), expect)
+
+
 def test_fold_small_integers_exact():
     """Integer-valued FP8 operands, power-of-two scales, K <= 512: fp32 sums are exact."""
     rng = np.random.default_rng(1)
