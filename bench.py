@@ -5,7 +5,8 @@ One step = the hot path over one batch:
   block-scaled GEMM vs W E4M3 [14336 x 4096] with 128x128 block scales
   (weights quantized once, offline, and resident) -> Out bf16 [4096 x 14336].
 value = 2*M*N*K / step time (TFLOP/s), summed over ranks. L2 is flushed
-(256 MB write) between timed steps; the flush is outside the per-step events.
+(256 MB write, then 256 MB read) between timed steps; the flush is outside the
+per-step events.
 
 Besides the headline, the JSON line carries per-kernel measurements of the
 other workloads of the same path (quantizer sweep, decode GEMMs, MXFP8 GEMM),
@@ -315,7 +316,10 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def _time_kernel(fn, flush, stream, reps):
+def _time_kernel(fn, flush, stream, reps, launches=1):
+    """Median event time of fn() (which enqueues `launches` kernels) after an L2
+    flush; the GPU hold before the start event scales with the number of
+    launches so that all of them are queued before it ends."""
     import torch
 
     for _ in range(3):
@@ -325,7 +329,7 @@ def _time_kernel(fn, flush, stream, reps):
     ts = []
     for _ in range(reps):
         flush()
-        hold_gpu()
+        hold_gpu(200_000 * launches)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -377,16 +381,31 @@ def measure_decode(args, fb, synth, dev, stream, flush, hbm_peak):
     wd = to_dev(synth.decode_w(Nd, Kd))
     qw, sw = fb.quantize(wd, fb.E4M3, fb.BLOCK_128x128)
     del wd
+    # back to back: one launch per weight copy (a decode step runs many GEMMs in a
+    # row); every copy is larger than L2, so each launch streams its W from HBM
+    n_copies = 8
+    copies = [(qw.clone(), sw.clone()) for _ in range(n_copies)]
     for m in (16, 64):
         xq, xs = fb.quantize(to_dev(synth.decode_x(m, Kd)), fb.E4M3, fb.TILE_1x128)
         o = torch.empty((m, Nd), dtype=torch.bfloat16, device=dev)
         t = _time_kernel(lambda: fb.gemm_blockscaled(xq, xs, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=o),
                          flush, stream, reps)
+
+        def seq():
+            for cw, cs in copies:
+                fb.gemm_blockscaled(xq, xs, fb.TILE_1x128, cw, cs, fb.BLOCK_128x128, out=o)
+
+        t_seq = _time_kernel(seq, flush, stream, max(5, reps // 2), launches=n_copies) / n_copies
         byts = Nd * Kd + m * Kd + m * Nd * 2 + 4 * (Kd // 128) * (m + Nd // 128)
-        res["decode_gemm_m%d" % m] = {"ms": round(t, 5), "GB/s": round(byts / (t * 1e-3) / 1e9, 1),
-                                      "frac_hbm": round(byts / (t * 1e-3) / 1e9 / hbm_peak, 4),
-                                      "TFLOP/s": round(2.0 * m * Nd * Kd / (t * 1e-3) / 1e12, 2),
-                                      "algorithmic_bytes": byts}
+        res["decode_gemm_m%d" % m] = {
+            "ms": round(t, 5), "GB/s": round(byts / (t * 1e-3) / 1e9, 1),
+            "frac_hbm": round(byts / (t * 1e-3) / 1e9 / hbm_peak, 4),
+            "TFLOP/s": round(2.0 * m * Nd * Kd / (t * 1e-3) / 1e12, 2), "algorithmic_bytes": byts,
+            "single_launch_note": "one launch between its own events (includes ~2.4 us of event-pair latency and the launch)",
+            "back_to_back": {"launches": n_copies, "weight_copies": n_copies, "ms_per_launch": round(t_seq, 5),
+                             "GB/s": round(byts / (t_seq * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(byts / (t_seq * 1e-3) / 1e9 / hbm_peak, 4)}}
+    del copies
     return res
 
 
