@@ -56,6 +56,16 @@ def lib():
         L.fp8_gemm_blockscaled_quantized_out.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp]
         L.fp8_gemm_mx.restype = i32
         L.fp8_gemm_mx.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
+        L.fp8_nvfp4_scales_bytes.restype = sz
+        L.fp8_nvfp4_scales_bytes.argtypes = [i64, i64, i32]
+        L.fp8_quantize_nvfp4.restype = i32
+        L.fp8_quantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, vp, sz, vp]
+        L.fp8_dequantize_nvfp4.restype = i32
+        L.fp8_dequantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp]
+        L.fp8_gemm_nvfp4.restype = i32
+        L.fp8_gemm_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+        L.fp8_debug_encode_e2m1_f32.restype = i32
+        L.fp8_debug_encode_e2m1_f32.argtypes = [vp, i64, vp, vp]
         L.fp8_debug_encode_f32.restype = i32
         L.fp8_debug_encode_f32.argtypes = [vp, i64, i32, vp, vp]
         L.fp8_debug_wait_probe.restype = i32
@@ -220,6 +230,62 @@ def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, st
     return out
 
 
+def nvfp4_scales_bytes(rows: int, cols: int, sf_layout: int = SF_TCGEN05) -> int:
+    return int(lib().fp8_nvfp4_scales_bytes(rows, cols, sf_layout))
+
+
+def quantize_nvfp4(x, sf_layout: int = SF_TCGEN05, static_tensor_scale=None, q=None, sf=None, tensor_scale=None,
+                   stream=None):
+    """NVFP4 quantize of bf16 x [rows x cols]: (codes uint8 [rows x cols/2], E4M3 block scales uint8,
+    tensor scale float32 [1]); static_tensor_scale: None (from this tensor's amax) or a device float32 [1]."""
+    import torch
+
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty(max(1, nvfp4_scales_bytes(rows, cols, sf_layout)), dtype=torch.uint8, device=dev)
+    if tensor_scale is None:
+        tensor_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = None
+    if static_tensor_scale is None:
+        ws = torch.empty(max(1, workspace_bytes(rows, cols, TENSOR)), dtype=torch.uint8, device=dev)
+    rc = lib().fp8_quantize_nvfp4(_ptr(x), rows, cols, x.stride(0), sf_layout, _ptr(static_tensor_scale), _ptr(q),
+                                  q.stride(0), _ptr(sf), _ptr(tensor_scale), _ptr(ws),
+                                  0 if ws is None else ws.numel(), _stream(stream))
+    _check(rc, "fp8_quantize_nvfp4")
+    return q, sf, tensor_scale
+
+
+def dequantize_nvfp4(q, sf, tensor_scale, cols: int, sf_layout: int = SF_TCGEN05, out=None, stream=None):
+    import torch
+
+    rows = q.shape[0]
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
+    rc = lib().fp8_dequantize_nvfp4(_ptr(q), rows, cols, q.stride(0), sf_layout, _ptr(sf), _ptr(tensor_scale),
+                                    _ptr(out), out.stride(0), _stream(stream))
+    _check(rc, "fp8_dequantize_nvfp4")
+    return out
+
+
+def gemm_nvfp4(a, a_sf, a_ts, b, b_sf, b_ts, out=None, status=None, stream=None):
+    """NVFP4 GEMM: a [M x K/2], b [N x K/2] packed codes, scales in SF_TCGEN05, tensor scales float32 [1]."""
+    import torch
+
+    M, Kh = a.shape
+    N, Kh2 = b.shape
+    assert Kh == Kh2 and a.is_contiguous() and b.is_contiguous()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    rc = lib().fp8_gemm_nvfp4(_ptr(a), _ptr(a_sf), _ptr(a_ts), _ptr(b), _ptr(b_sf), _ptr(b_ts), _ptr(out), M, N,
+                              2 * Kh, _ptr(status), _stream(stream))
+    _check(rc, "fp8_gemm_nvfp4")
+    return out
+
+
 def debug_encode_f32(x, fmt: int, out=None, stream=None):
     """RNE-satfinite encode of fp32 values (the quantizers' element step, scale 1)."""
     import torch
@@ -228,6 +294,17 @@ def debug_encode_f32(x, fmt: int, out=None, stream=None):
     if out is None:
         out = torch.empty(x.numel(), dtype=torch.uint8, device=x.device)
     _check(lib().fp8_debug_encode_f32(_ptr(x), x.numel(), fmt, _ptr(out), _stream(stream)), "fp8_debug_encode_f32")
+    return out
+
+
+def debug_encode_e2m1_f32(x, out=None, stream=None):
+    """E2M1 codes (one per byte) of fp32 values: NVFP4's element step with scale 1."""
+    import torch
+
+    assert x.dtype == torch.float32 and x.is_contiguous()
+    if out is None:
+        out = torch.empty(x.numel(), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_debug_encode_e2m1_f32(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "fp8_debug_encode_e2m1_f32")
     return out
 
 

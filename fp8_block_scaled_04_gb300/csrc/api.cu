@@ -283,6 +283,79 @@ fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void 
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t fp8_nvfp4_scales_bytes(int64_t rows, int64_t cols, fp8_sf_layout_t sf_layout) {
+  if (rows < 0 || cols < 0 || cols % 16 || rows > kMaxDim || cols > kMaxDim) return 0;
+  const int64_t ng = cols / 16;
+  if (sf_layout == FP8_SF_LINEAR) return static_cast<size_t>(rows * ng);
+  if (sf_layout == FP8_SF_TCGEN05) return static_cast<size_t>(((rows + 127) / 128) * ((ng + 3) / 4) * 512);
+  return 0;
+}
+
+fp8_status_t fp8_quantize_nvfp4(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x,
+                                fp8_sf_layout_t sf_layout, const float *static_tensor_scale_dev, void *q_out_dev,
+                                int64_t ld_q, void *sf_out_dev, float *tensor_scale_out_dev, void *workspace_dev,
+                                size_t workspace_bytes, fp8_stream_t stream) {
+  if (sf_layout != FP8_SF_LINEAR && sf_layout != FP8_SF_TCGEN05) return FP8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim || cols % 16) return FP8_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (x_dev == nullptr || q_out_dev == nullptr || sf_out_dev == nullptr || tensor_scale_out_dev == nullptr)
+    return FP8_ERR_INVALID_ARG;
+  if (ld_x < cols || ld_q < cols / 2) return FP8_ERR_INVALID_ARG;
+  if (!aligned(x_dev, 16) || ld_x % 8 || !aligned(q_out_dev, 8) || ld_q % 8 || !aligned(tensor_scale_out_dev, 4))
+    return FP8_ERR_ALIGNMENT;
+  if (static_tensor_scale_dev != nullptr) {
+    if (!aligned(static_tensor_scale_dev, 4)) return FP8_ERR_ALIGNMENT;
+  } else {
+    if (workspace_dev == nullptr || workspace_bytes < fp8_quantize_workspace_bytes(rows, cols, FP8_GRAN_TENSOR))
+      return FP8_ERR_WORKSPACE;
+    if (!aligned(workspace_dev, 4)) return FP8_ERR_ALIGNMENT;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool tiled = sf_layout == FP8_SF_TCGEN05;
+  if (tiled && (rows % 128 || (cols / 16) % 4)) {
+    // padding bytes of partial atoms are 0 (scale 0)
+    if (cudaMemsetAsync(sf_out_dev, 0, fp8_nvfp4_scales_bytes(rows, cols, sf_layout), s) != cudaSuccess)
+      return FP8_ERR_CUDA;
+  }
+  return launch_quantize_nvfp4(static_cast<const uint16_t *>(x_dev), rows, cols, ld_x, tiled,
+                               static_tensor_scale_dev, static_cast<uint8_t *>(q_out_dev), ld_q,
+                               static_cast<uint8_t *>(sf_out_dev), tensor_scale_out_dev,
+                               static_cast<uint32_t *>(workspace_dev), s);
+}
+
+fp8_status_t fp8_dequantize_nvfp4(const void *q_dev, int64_t rows, int64_t cols, int64_t ld_q,
+                                  fp8_sf_layout_t sf_layout, const void *sf_dev, const float *tensor_scale_dev,
+                                  void *out_dev, int64_t ld_out, fp8_stream_t stream) {
+  if (sf_layout != FP8_SF_LINEAR && sf_layout != FP8_SF_TCGEN05) return FP8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim || cols % 16) return FP8_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0 || cols == 0) return FP8_OK;
+  if (q_dev == nullptr || sf_dev == nullptr || tensor_scale_dev == nullptr || out_dev == nullptr)
+    return FP8_ERR_INVALID_ARG;
+  if (ld_q < cols / 2 || ld_out < cols) return FP8_ERR_INVALID_ARG;
+  if (!aligned(q_dev, 8) || ld_q % 8 || !aligned(out_dev, 16) || ld_out % 8 || !aligned(tensor_scale_dev, 4))
+    return FP8_ERR_ALIGNMENT;
+  return launch_dequantize_nvfp4(static_cast<const uint8_t *>(q_dev), rows, cols, ld_q,
+                                 sf_layout == FP8_SF_TCGEN05, static_cast<const uint8_t *>(sf_dev), tensor_scale_dev,
+                                 static_cast<uint16_t *>(out_dev), ld_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_gemm_nvfp4(const void *a_dev, const void *a_sf_dev, const float *a_ts_dev, const void *b_dev,
+                            const void *b_sf_dev, const float *b_ts_dev, void *out_dev, int64_t M, int64_t N,
+                            int64_t K, int *dev_status, fp8_stream_t stream) {
+  fp8_status_t st = check_gemm_common(a_dev, b_dev, out_dev, M, N, K, FP8_E4M3, FP8_E4M3);
+  if (st != FP8_OK || M == 0 || N == 0) return st;
+  if (K % 256) return FP8_ERR_UNSUPPORTED_SHAPE;
+  if (a_sf_dev == nullptr || b_sf_dev == nullptr || a_ts_dev == nullptr || b_ts_dev == nullptr)
+    return FP8_ERR_INVALID_ARG;
+  if (!aligned(a_sf_dev, 16) || !aligned(b_sf_dev, 16) || !aligned(a_ts_dev, 4) || !aligned(b_ts_dev, 4))
+    return FP8_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return FP8_ERR_ALIGNMENT;
+  return launch_gemm_nvfp4(static_cast<const uint8_t *>(a_dev), static_cast<const uint8_t *>(a_sf_dev), a_ts_dev,
+                           static_cast<const uint8_t *>(b_dev), static_cast<const uint8_t *>(b_sf_dev), b_ts_dev,
+                           static_cast<uint16_t *>(out_dev), M, N, K, dev_status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
 fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fmt, void *out_dev,
                                   fp8_stream_t stream) {
   if (!valid_fmt(fmt) || n < 0 || n % 8) return FP8_ERR_INVALID_ARG;
@@ -290,6 +363,14 @@ fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fm
   if (x_dev == nullptr || out_dev == nullptr) return FP8_ERR_INVALID_ARG;
   if (!aligned(x_dev, 16) || !aligned(out_dev, 8)) return FP8_ERR_ALIGNMENT;
   return launch_encode_f32(x_dev, n, fmt, static_cast<uint8_t *>(out_dev), reinterpret_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_debug_encode_e2m1_f32(const float *x_dev, int64_t n, void *out_dev, fp8_stream_t stream) {
+  if (n < 0 || n % 8) return FP8_ERR_INVALID_ARG;
+  if (n == 0) return FP8_OK;
+  if (x_dev == nullptr || out_dev == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(x_dev, 16) || !aligned(out_dev, 8)) return FP8_ERR_ALIGNMENT;
+  return launch_encode_e2m1(x_dev, n, static_cast<uint8_t *>(out_dev), reinterpret_cast<cudaStream_t>(stream));
 }
 
 fp8_status_t fp8_debug_wait_probe(int *dev_status, uint64_t timeout_ns, fp8_stream_t stream) {

@@ -14,12 +14,15 @@
 //   MMA group into a fresh tensor-memory buffer; the consumer warps fold it
 //   into fp32 registers as acc += (s_x[m,kb] * s_w[n/128,kb]) * partial. Two
 //   tensor-memory buffers let the MMA of chunk kb+1 run while chunk kb folds.
-// gemm_tmem_kernel<false> -- per-tensor / per-token / per-channel scales: the
-//   whole K sum stays in tensor memory and the scale product is applied once
-//   in the epilogue.
-// gemm_tmem_kernel<true> -- MXFP8: kind::mxf8f6f4.block_scale applies one
+// gemm_tmem_kernel<KIND_EPI> -- per-tensor / per-token / per-channel scales:
+//   the whole K sum stays in tensor memory and the scale product is applied
+//   once in the epilogue.
+// gemm_tmem_kernel<KIND_MX8> -- MXFP8: kind::mxf8f6f4.block_scale applies one
 //   UE8M0 scale per 32 K-elements inside the tensor core ("Low precision",
 //   microscaling); scale-factor atoms go smem -> tensor memory with tcgen05.cp.
+// gemm_tmem_kernel<KIND_NVF4> -- NVFP4: kind::mxf4nvf4.block_scale.scale_vec::4X
+//   with E2M1 operands and one E4M3 scale per 16 K-elements; the two fp32
+//   tensor scales multiply the accumulator in the epilogue.
 //
 // Every barrier wait is bounded (see mbar_wait): on expiry the CTA records
 // FP8_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees tensor memory
@@ -1133,33 +1136,43 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
 }
 
 // =====================================================================
-// Tensor-memory accumulating kernel: epilogue-scaled (MX = false) or
-// block-scaled MXFP8 (MX = true)
+// Tensor-memory accumulating kernel: epilogue-scaled (KIND_EPI), block-scaled
+// MXFP8 (KIND_MX8: UE8M0 scale per 32 K) or NVFP4 (KIND_NVF4: E2M1 operands,
+// E4M3 scale per 16 K, fp32 tensor scales applied in the epilogue)
 // =====================================================================
-template <bool MX, int BN, int STAGES, int NACC>
+constexpr int KIND_EPI = 0, KIND_MX8 = 1, KIND_NVF4 = 2;
+
+// A stage always holds 128 bytes of K per row: 128 fp8 or 256 fp4 elements.
+// Scale atoms (128 rows x 4 scales, 512 bytes) per stage and 128-row block:
+// one for MXFP8 (4 x 32 K), four for NVFP4 (4 x 4 x 16 K).
+template <int KIND, int BN, int STAGES, int NACC>
 struct AccCfg {
+  static constexpr bool MX = KIND != KIND_EPI;
+  static constexpr int ATOMS = KIND == KIND_NVF4 ? 4 : (MX ? 1 : 0);
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
-  static constexpr int SFA_BYTES = MX ? 512 : 0;               // one 128x4 atom
-  static constexpr int SFB_BYTES = MX ? 512 * (BN / 128) : 0;  // BN/128 atoms
+  static constexpr int SFA_BYTES = 512 * ATOMS;
+  static constexpr int SFB_BYTES = 512 * ATOMS * (BN / 128);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
   static constexpr int CONSUMER_WARPS = 4 * (BN / 128);
   static constexpr int THREADS = 64 + 32 * CONSUMER_WARPS;
-  static constexpr int SF_COLS = MX ? 4 + 4 * (BN / 128) : 0;  // tensor-memory columns per stage
+  static constexpr int SF_COLS = 4 * ATOMS * (1 + BN / 128);  // tensor-memory columns per stage
   static constexpr int ACC_COLS = NACC * BN;                    // NACC accumulators (2: epilogue overlaps MMA)
   static constexpr uint32_t TMEM_COLS = ACC_COLS + STAGES * SF_COLS <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_STRIDE + 1024;
   static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory budget");
 };
 
-template <bool MX, int BN, int STAGES, int NACC>
-__global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
+template <int KIND, int BN, int STAGES, int NACC>
+__global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
     gemm_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float *__restrict__ sa, int sa_per_row, const float *__restrict__ sb, int sb_per_col,
                      const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ out,
                      int M, int N, int K, uint32_t idesc, int *dev_status, int group_m) {
-  using C = AccCfg<MX, BN, STAGES, NACC>;
+  using C = AccCfg<KIND, BN, STAGES, NACC>;
+  constexpr bool MX = C::MX;
+  constexpr bool F4 = KIND == KIND_NVF4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   __shared__ uint64_t full[STAGES], empty[STAGES], afull[NACC], aempty[NACC], drain;
@@ -1167,7 +1180,8 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int KB = (K + BK - 1) / BK;
+  // k-blocks of 128 bytes per row (K % 256 == 0 for NVFP4)
+  const int KB = F4 ? K / 256 : (K + BK - 1) / BK;
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
   const int ntiles = num_m * num_n;
@@ -1215,14 +1229,16 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
           tma_load_2d(st, &tmA, kb * BK, mt * BM, &full[s]);
           tma_load_2d(st + C::A_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
           if (MX) {
-            // scale-factor atoms: [row block][K/128 block] x 512 bytes
-            bulk_load(st + C::A_BYTES + C::B_BYTES, sfa + (static_cast<int64_t>(mt) * KB + kb) * 512, 512, &full[s]);
+            // scale-factor atoms: [row block][atom along K] x 512 bytes; a
+            // stage's atoms of one 128-row block are contiguous
+            constexpr int AB = 512 * C::ATOMS;
+            bulk_load(st + C::A_BYTES + C::B_BYTES, sfa + (static_cast<int64_t>(mt) * KB + kb) * AB, AB, &full[s]);
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j) {
               int nb = nt * (BN / 128) + j;
               nb = nb < nblk128_b ? nb : nblk128_b - 1;  // rows past N are zero; any finite scale will do
-              bulk_load(st + C::A_BYTES + C::B_BYTES + 512 + 512 * j,
-                        sfb + (static_cast<int64_t>(nb) * KB + kb) * 512, 512, &full[s]);
+              bulk_load(st + C::A_BYTES + C::B_BYTES + AB + AB * j, sfb + (static_cast<int64_t>(nb) * KB + kb) * AB,
+                        AB, &full[s]);
             }
           }
         }
@@ -1254,7 +1270,26 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + s * C::STAGE_STRIDE);
           const uint32_t b0 = a0 + C::A_BYTES;
-          if (MX) {
+          if (F4) {
+            // NVFP4: one scale atom per MMA (K = 64, four 16-element scales per
+            // row); A's atom k at column +4k, B's at +8k (second 128-row block
+            // of B at +4, as the block-scaled MMA reads a 256-row B)
+            const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
+            const uint32_t sfb_t = sfa_t + 16;
+            const uint32_t sf_smem = b0 + C::B_BYTES;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              tmem_cp_32x128b_warpx4(sfa_t + 4 * k, sdesc_plain_32x16(sf_smem + 512 * k));
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j)
+                tmem_cp_32x128b_warpx4(sfb_t + 8 * k + 4 * j,
+                                       sdesc_plain_32x16(sf_smem + 2048 + 2048 * j + 512 * k));
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_mxf4nvf4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, sfa_t + 4 * k,
+                           sfb_t + 8 * k, (kb > 0 || k > 0) ? 1u : 0u);
+          } else if (MX) {
             const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + 4;
             const uint32_t sf_smem = b0 + C::B_BYTES;
@@ -1325,7 +1360,12 @@ __global__ void __launch_bounds__(AccCfg<MX, BN, STAGES, NACC>::THREADS, 1)
         const int nc = n0 + 32 * c;
         if (row_ok && nc < N) {
           float v[32];
-          if (MX) {
+          if (F4) {
+            // the two fp32 tensor scales (sa, sb point at them)
+            const float g = __ldg(sa) * __ldg(sb);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]) * g;
+          } else if (MX) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]);
           } else if (sb_per_col) {
@@ -1571,10 +1611,10 @@ fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool
                                          const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,
                                          int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {
   constexpr int BN = 256, ST = 4, NACC = 2;
-  using C = AccCfg<false, BN, ST, NACC>;
+  using C = AccCfg<KIND_EPI, BN, ST, NACC>;
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-  auto kern = gemm_tmem_kernel<false, BN, ST, NACC>;
+  auto kern = gemm_tmem_kernel<KIND_EPI, BN, ST, NACC>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
@@ -1588,15 +1628,37 @@ fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t 
                             int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
                             cudaStream_t stream) {
   constexpr int BN = MX_BN, ST = MX_STAGES, NACC = MX_NACC;
-  using C = AccCfg<true, BN, ST, NACC>;
+  using C = AccCfg<KIND_MX8, BN, ST, NACC>;
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-  auto kern = gemm_tmem_kernel<true, BN, ST, NACC>;
+  auto kern = gemm_tmem_kernel<KIND_MX8, BN, ST, NACC>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
       ta, tb, nullptr, 0, nullptr, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
       idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status, raster_group(M, K));
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// NVFP4: a and b are packed E2M1 [M x K/2], [N x K/2] bytes (K % 256 == 0);
+// sfa, sfb the E4M3 block scales in the tiled layout (K/16 groups per row); ta,
+// tb the fp32 tensor scales (device memory).
+fp8_status_t launch_gemm_nvfp4(const uint8_t *a, const uint8_t *sfa, const float *ta, const uint8_t *b,
+                               const uint8_t *sfb, const float *tb, uint16_t *out, int64_t M, int64_t N, int64_t K,
+                               int *dev_status, cudaStream_t stream) {
+  constexpr int BN = 256, ST = 4, NACC = 1;
+  using C = AccCfg<KIND_NVF4, BN, ST, NACC>;
+  CUtensorMap tma, tmb;
+  const int64_t kbytes = K / 2;
+  if (!make_tmap_u8(&tma, a, M, kbytes, kbytes, BM, BK) || !make_tmap_u8(&tmb, b, N, kbytes, kbytes, BN, BK))
+    return FP8_ERR_CUDA;
+  auto kern = gemm_tmem_kernel<KIND_NVF4, BN, ST, NACC>;
+  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+  const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
+  kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
+      tma, tmb, ta, 0, tb, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+      idesc_mxf4nvf4(BM, BN), dev_status, raster_group(M, kbytes));
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }

@@ -62,6 +62,23 @@ fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t 
 
 fp8_status_t launch_wait_probe(int *dev_status, uint64_t timeout_ns, cudaStream_t stream);
 
+// amax pass of the per-tensor quantizers (cols % 8 == 0, 16-byte aligned rows)
+fp8_status_t launch_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint32_t *amax_bits,
+                         cudaStream_t stream);
+
+// NVFP4 (nvfp4.cu): codes [rows x cols/2] bytes, E4M3 block scales (tiled or
+// linear [rows][cols/16]), fp32 tensor scale in device memory.
+fp8_status_t launch_quantize_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, bool tiled,
+                                   const float *static_ts, uint8_t *q, int64_t ld_q, uint8_t *sf, float *ts_out,
+                                   uint32_t *amax_ws, cudaStream_t stream);
+fp8_status_t launch_dequantize_nvfp4(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, bool tiled,
+                                     const uint8_t *sf, const float *ts, uint16_t *out, int64_t ld_out,
+                                     cudaStream_t stream);
+fp8_status_t launch_encode_e2m1(const float *x, int64_t n, uint8_t *out, cudaStream_t stream);
+fp8_status_t launch_gemm_nvfp4(const uint8_t *a, const uint8_t *sfa, const float *ta, const uint8_t *b,
+                               const uint8_t *sfb, const float *tb, uint16_t *out, int64_t M, int64_t N, int64_t K,
+                               int *dev_status, cudaStream_t stream);
+
 // 2-D tensor map over a row-major uint8 matrix [rows x cols] (cols contiguous,
 // row stride ld bytes), box = box_cols x box_rows, 128-byte swizzle.
 bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,

@@ -738,6 +738,16 @@ static fp8_status_t noalloc_scratch_address(void **out) {
   return FP8_OK;
 }
 
+// The amax pass alone (fp32 bits of max |x| reduced into *amax_bits, which the
+// caller zeroes), for quantizers in other files.
+fp8_status_t launch_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint32_t *amax_bits,
+                         cudaStream_t stream) {
+  const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
+  amax_kernel<<<stream_grid(tasks), kThreads, 0, stream>>>(x, rows, cols, ld_x, amax_bits);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 fp8_status_t launch_quantize_tensor_noalloc(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                                             uint8_t *q, int64_t ld_q, float *scale_out, size_t scratch_needed,
                                             cudaStream_t stream) {

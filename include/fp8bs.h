@@ -226,6 +226,62 @@ fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void 
                          fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
                          int *dev_status, fp8_stream_t stream);
 
+/* ------------------------------------------------------------------ NVFP4
+ * "Low precision: FP8, FP4, and microscaling" (NVFP4 paragraph): blocks of 16
+ * elements, an E4M3 microscale per block and one fp32 scale per tensor that
+ * keeps the microscales inside E4M3's range. The page prints neither the FP4
+ * element format nor the scale arithmetic; this library takes:
+ *   element: FP4 E2M1 (the OCP Microscaling element format the page cites):
+ *     sign, 2 exponent bits (bias 1), 1 mantissa bit; +-{0,0.5,1,1.5,2,3,4,6};
+ *     round to nearest even, saturating at +-6; codes packed two per byte,
+ *     element 2i in the low nibble of byte i of its row;
+ *   s_t = fp32(amax_tensor / 2688)  (2688 = 6 * 448; 1 when that is 0 or not
+ *     finite);
+ *   per block of 16 consecutive elements of a row:
+ *     s_b = E4M3(fp32(fp32(amax_block / 6) / s_t))   (stored as its E4M3 code),
+ *     S = fp32(s_b * s_t), S_inv = fp32(1 / S) (0 if S = 0 or 1/S not finite),
+ *     q = E2M1(fp32(x * S_inv));
+ *   value: decode(q) * s_b * s_t.
+ * Block scales (uint8 E4M3 codes, one per 16 elements): FP8_SF_LINEAR =
+ * uint8[rows][cols/16]; FP8_SF_TCGEN05 = the 128x4-atom layout described above
+ * for MX, with cols/16 groups per row (each atom covers 64 elements of K);
+ * padding bytes are 0. */
+
+/* Bytes of the NVFP4 block-scale array for [rows x cols], or 0 if invalid. */
+size_t fp8_nvfp4_scales_bytes(int64_t rows, int64_t cols, fp8_sf_layout_t sf_layout);
+
+/* Quantize bf16 [rows x cols] (leading dimension ld_x elements) to NVFP4.
+ * q_out_dev: uint8 [rows x cols/2], leading dimension ld_q bytes (>= cols/2,
+ * multiple of 8). sf_out_dev: fp8_nvfp4_scales_bytes bytes. tensor_scale_out_dev:
+ * one device float, s_t. static_tensor_scale_dev: NULL (s_t from this tensor's
+ * amax: two passes, workspace of fp8_quantize_workspace_bytes(rows, cols,
+ * FP8_GRAN_TENSOR) bytes) or a device float used as s_t (one pass, no
+ * workspace). Rules: cols % 16 == 0; x_dev 16-byte aligned, ld_x % 8 == 0;
+ * q_out_dev 8-byte aligned. */
+fp8_status_t fp8_quantize_nvfp4(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x,
+                                fp8_sf_layout_t sf_layout, const float *static_tensor_scale_dev, void *q_out_dev,
+                                int64_t ld_q, void *sf_out_dev, float *tensor_scale_out_dev, void *workspace_dev,
+                                size_t workspace_bytes, fp8_stream_t stream);
+
+/* out = bf16(fp32(decode(q) * fp32(s_b * s_t))), bf16 [rows x cols], leading
+ * dimension ld_out elements (multiple of 8, out 16-byte aligned). Same q and
+ * scale layouts as fp8_quantize_nvfp4; tensor_scale_dev: device float s_t. */
+fp8_status_t fp8_dequantize_nvfp4(const void *q_dev, int64_t rows, int64_t cols, int64_t ld_q,
+                                  fp8_sf_layout_t sf_layout, const void *sf_dev, const float *tensor_scale_dev,
+                                  void *out_dev, int64_t ld_out, fp8_stream_t stream);
+
+/* NVFP4 GEMM on the tensor core's block-scaled MMA
+ * (tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X): Out[m][n] =
+ * a_ts * b_ts * sum_k E2M1(a[m][k]) s_b(a; m, k/16) E2M1(b[n][k]) s_b(b; n, k/16),
+ * fp32 accumulation over all of K, bf16 out [M x N]. a_dev [M x K/2] and
+ * b_dev [N x K/2] packed codes (leading dimension K/2 bytes); a_sf_dev /
+ * b_sf_dev block scales in the FP8_SF_TCGEN05 layout; a_ts_dev / b_ts_dev the
+ * device fp32 tensor scales. Rules: K % 256 == 0, N % 16 == 0; a_dev, b_dev,
+ * out_dev, a_sf_dev, b_sf_dev 16-byte aligned. dev_status as above. */
+fp8_status_t fp8_gemm_nvfp4(const void *a_dev, const void *a_sf_dev, const float *a_ts_dev, const void *b_dev,
+                            const void *b_sf_dev, const float *b_ts_dev, void *out_dev, int64_t M, int64_t N,
+                            int64_t K, int *dev_status, fp8_stream_t stream);
+
 /* Codec check (no counterpart on the pages beyond the element step itself):
  * out[i] = RNE_satfinite(x[i]) in `fmt`, computed by the same device routine
  * the quantizers use for their last step ("Low precision", qdq_e4m3 listing:
@@ -234,6 +290,13 @@ fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void 
  * (8-byte aligned), n % 8 == 0. */
 fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fmt, void *out_dev,
                                   fp8_stream_t stream);
+
+/* Codec check for NVFP4's element step (same role as fp8_debug_encode_f32):
+ * out[i] = the E2M1 code (low 4 bits of byte i) of x[i], rounded to nearest
+ * even and saturated at +-6 by the device routine fp8_quantize_nvfp4 uses.
+ * x_dev fp32 [n] (16-byte aligned), out_dev uint8 [n] (8-byte aligned),
+ * n % 8 == 0. */
+fp8_status_t fp8_debug_encode_e2m1_f32(const float *x_dev, int64_t n, void *out_dev, fp8_stream_t stream);
 
 /* Check of the bounded-wait machinery the GEMM kernels use (no counterpart on
  * the pages): launches one CTA that waits on a barrier nothing ever arrives

@@ -69,6 +69,25 @@ def lib():
         L.orc_quantize_delayed.argtypes = [vp, c_i64, c_i64, c_int, vp, c_int, c_int, c_int, vp, vp, vp, c_int]
         L.orc_default_threads.restype = c_int
         L.orc_default_threads.argtypes = []
+        L.orc_e2m1_decode.restype = ctypes.c_double
+        L.orc_e2m1_decode.argtypes = [ctypes.c_uint32]
+        L.orc_e2m1_encode_nearest.restype = ctypes.c_uint8
+        L.orc_e2m1_encode_nearest.argtypes = [ctypes.c_float]
+        L.orc_e2m1_encode_binade.restype = ctypes.c_uint8
+        L.orc_e2m1_encode_binade.argtypes = [ctypes.c_float]
+        L.orc_e2m1_encoders_disagree.restype = c_i64
+        L.orc_e2m1_encoders_disagree.argtypes = [c_u64, c_u64, c_int, ctypes.POINTER(c_u64)]
+        L.orc_e2m1_check_codes.restype = c_i64
+        L.orc_e2m1_check_codes.argtypes = [c_u64, c_u64, vp, c_int, ctypes.POINTER(c_u64)]
+        L.orc_nvfp4_tensor_scale.restype = ctypes.c_float
+        L.orc_nvfp4_tensor_scale.argtypes = [ctypes.c_float]
+        L.orc_quantize_nvfp4.restype = c_int
+        L.orc_quantize_nvfp4.argtypes = [vp, c_i64, c_i64, c_i64, c_int, vp, vp, vp, vp]
+        L.orc_dequantize_nvfp4.restype = c_int
+        L.orc_dequantize_nvfp4.argtypes = [vp, vp, c_int, ctypes.c_float, c_i64, c_i64, vp]
+        L.orc_gemm_nvfp4.restype = c_int
+        L.orc_gemm_nvfp4.argtypes = [vp, vp, ctypes.c_float, vp, vp, ctypes.c_float, c_int, c_i64, c_i64, c_i64,
+                                     vp, c_i64, vp, c_i64, vp, vp]
         _lib = L
     return _lib
 
@@ -243,4 +262,86 @@ def gemm(a_q, a_scales, a_gran, b_q, b_scales, b_gran, a_fmt=E4M3, b_fmt=E4M3, a
                         _p(r), nr, _p(c), nc, _p(ref), _p(bound), nthreads)
     if rc != 0:
         raise ValueError("oracle gemm failed (rc=%d)" % rc)
+    return ref, bound
+
+
+# ---------------------------------------------------------------- NVFP4
+# "Low precision: FP8, FP4, and microscaling": blocks of 16, E4M3 microscale
+# per block, one fp32 scale per tensor. Element format and scale arithmetic
+# are readings stated in oracle.c (NVFP4 section).
+def e2m1_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint32).ravel()
+    return np.array([lib().orc_e2m1_decode(int(v)) for v in c], dtype=np.float64).reshape(np.shape(codes))
+
+
+def e2m1_encode_nearest(x: float) -> int:
+    return int(lib().orc_e2m1_encode_nearest(float(x)))
+
+
+def e2m1_encode_binade(x: float) -> int:
+    return int(lib().orc_e2m1_encode_binade(float(x)))
+
+
+def e2m1_encoders_disagree(start: int, count: int, nthreads: int = 0):
+    first = ctypes.c_uint64(0)
+    bad = lib().orc_e2m1_encoders_disagree(start, count, nthreads, ctypes.byref(first))
+    return int(bad), int(first.value)
+
+
+def e2m1_check_codes(start: int, codes: np.ndarray, nthreads: int = 0):
+    """(mismatches, first mismatching fp32 pattern) of E2M1 codes for patterns start.. ."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    first = ctypes.c_uint64(0)
+    bad = lib().orc_e2m1_check_codes(start, c.size, _p(c), nthreads, ctypes.byref(first))
+    return int(bad), int(first.value)
+
+
+def nvfp4_tensor_scale(amax: float) -> float:
+    return float(lib().orc_nvfp4_tensor_scale(float(amax)))
+
+
+def quantize_nvfp4(x_bf16: np.ndarray, sf_layout: int = SF_TILED, static_tensor_scale=None):
+    """x: uint16 bf16 bits [rows x cols], cols % 16 == 0. Returns (q [rows x cols/2] uint8,
+    sf uint8 E4M3 codes (tiled or linear [rows][cols/16]), tensor scale float)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, cols = x.shape
+    q = np.zeros((rows, cols // 2), dtype=np.uint8)
+    ng = cols // 16
+    sf = np.zeros(mx_tiled_bytes(rows, ng) if sf_layout == SF_TILED else rows * ng, dtype=np.uint8)
+    st = np.zeros(1, dtype=np.float32)
+    stat = None if static_tensor_scale is None else np.array([static_tensor_scale], dtype=np.float32)
+    rc = lib().orc_quantize_nvfp4(_p(x), rows, cols, cols, sf_layout, _p(stat), _p(q), _p(sf), _p(st))
+    if rc != 0:
+        raise ValueError("orc_quantize_nvfp4 failed: %d" % rc)
+    return q, sf, float(st[0])
+
+
+def dequantize_nvfp4(q, sf, tensor_scale: float, cols: int, sf_layout: int = SF_TILED) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    rows = q.shape[0]
+    out = np.zeros((rows, cols), dtype=np.uint16)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    rc = lib().orc_dequantize_nvfp4(_p(q), _p(sf), sf_layout, float(tensor_scale), rows, cols, _p(out))
+    if rc != 0:
+        raise ValueError("orc_dequantize_nvfp4 failed: %d" % rc)
+    return out
+
+
+def gemm_nvfp4(a_q, a_sf, a_ts, b_q, b_sf, b_ts, sf_layout: int = SF_TILED, rows=None, cols=None):
+    """fp64 reference and bound of X_hat W_hat^T for NVFP4 operands (packed [M x K/2], [N x K/2])."""
+    a_q = np.ascontiguousarray(a_q, dtype=np.uint8)
+    b_q = np.ascontiguousarray(b_q, dtype=np.uint8)
+    M, K = a_q.shape[0], a_q.shape[1] * 2
+    N = b_q.shape[0]
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else len(r)
+    nc = N if c is None else len(c)
+    ref = np.zeros((nr, nc), dtype=np.float64)
+    bound = np.zeros((nr, nc), dtype=np.float64)
+    rc = lib().orc_gemm_nvfp4(_p(a_q), _p(np.ascontiguousarray(a_sf, dtype=np.uint8)), float(a_ts), _p(b_q),
+                              _p(np.ascontiguousarray(b_sf, dtype=np.uint8)), float(b_ts), sf_layout, M, N, K,
+                              _p(r), nr, _p(c), nc, _p(ref), _p(bound))
+    if rc != 0:
+        raise ValueError("orc_gemm_nvfp4 failed: %d" % rc)
     return ref, bound

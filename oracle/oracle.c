@@ -749,3 +749,285 @@ int orc_gemm(const uint8_t *a, int64_t lda, const void *sa, int a_gran, int a_sf
   free(ahat);
   return 0;
 }
+
+/* ================================================================== */
+/* NVFP4 ([LowPrec] "Low precision: FP8, FP4, and microscaling": NVFP4   */
+/* uses blocks of 16 elements, an E4M3 microscale per block and one FP32 */
+/* scale per tensor that keeps the microscales inside E4M3's range).     */
+/*                                                                        */
+/* Readings (the page names FP4 and NVFP4 but prints neither the element */
+/* format nor the scale arithmetic):                                      */
+/*  - the element format is FP4 E2M1 of the OCP Microscaling spec the     */
+/*    page cites: sign, 2 exponent bits (bias 1), 1 mantissa bit; values  */
+/*    +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}; no infinity or NaN; encoding rounds */
+/*    to nearest, ties to the even code, and saturates at +-6;           */
+/*  - tensor scale s_t = fp32(amax_t / (6 * 448)), so that a block holding */
+/*    the tensor's amax gets microscale 448 (E4M3's largest value); 1 when */
+/*    it comes out 0 or non-finite;                                       */
+/*  - block microscale: u = fp32(fp32(amax_b / 6) / s_t), stored as the   */
+/*    E4M3 code of u (the FP8 encoder above); s_b = its value (>= 0);     */
+/*  - element: S = fp32(s_b * s_t), S_inv = fp32(1 / S) (0 when S is 0 or */
+/*    1/S is not finite), q = E2M1(fp32(x * S_inv)), as the 8-bit path     */
+/*    multiplies by a precomputed inverse;                                */
+/*  - dequantized value: decode(q) * s_b * s_t.                           */
+/* ================================================================== */
+
+/* E2M1 code (4 bits) -> value. */
+double orc_e2m1_decode(uint32_t c) {
+  const int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -v : v;
+}
+
+/* Nearest representable value by comparison with the midpoints between
+   neighbouring magnitudes; a tie takes the code whose mantissa bit is 0. */
+uint8_t orc_e2m1_encode_nearest(float xf) {
+  const uint8_t sign = signbit(xf) ? 8u : 0u;
+  const double a = fabs((double)xf);
+  if (isnan(xf)) return 0x7u; /* no NaN in E2M1: not produced for finite inputs */
+  uint8_t code = 7;            /* saturate */
+  for (uint8_t c = 0; c < 7; ++c) {
+    const double lo = orc_e2m1_decode(c), hi = orc_e2m1_decode(c + 1u);
+    const double mid = 0.5 * (lo + hi);
+    if (a < mid) {
+      code = c;
+      break;
+    }
+    if (a == mid) {
+      code = (c & 1u) ? (uint8_t)(c + 1u) : c;
+      break;
+    }
+  }
+  return (uint8_t)(sign | code);
+}
+
+/* The same rounding derived arithmetically: find the binade of |x|, scale the
+   significand to one fraction bit, round half to even, then saturate. */
+uint8_t orc_e2m1_encode_binade(float xf) {
+  const uint8_t sign = signbit(xf) ? 8u : 0u;
+  if (isnan(xf)) return 0x7u;
+  double a = fabs((double)xf);
+  if (a >= 6.0) return (uint8_t)(sign | 7u);
+  int e;
+  (void)frexp(a, &e);      /* a = f * 2^e, f in [0.5, 1) */
+  int ub = e - 1;          /* unbiased exponent of a (a in [2^ub, 2^(ub+1))) */
+  if (ub < 0) ub = 0;      /* below 1: the subnormal spacing 0.5 */
+  const double step = ldexp(0.5, ub); /* one fraction bit */
+  double n = a / step;                /* in [0, 4) units of step */
+  double r = floor(n);
+  const double frac = n - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  double v = r * step;
+  if (v > 6.0) v = 6.0;
+  for (uint8_t c = 0; c < 8; ++c)
+    if (orc_e2m1_decode(c) == v) return (uint8_t)(sign | c);
+  return (uint8_t)(sign | 7u);
+}
+
+#define E2M1_MAXT 256
+typedef struct {
+  uint64_t start;
+  int64_t bad[E2M1_MAXT];
+  uint64_t first[E2M1_MAXT];
+} e2m1_cmp;
+
+static void e2m1_cmp_range(void *p, int64_t lo, int64_t hi, int tid) {
+  e2m1_cmp *c = (e2m1_cmp *)p;
+  for (int64_t j = lo; j < hi; ++j) {
+    const uint32_t u = (uint32_t)(c->start + (uint64_t)j);
+    float f;
+    memcpy(&f, &u, 4);
+    if (isnan(f)) continue;
+    if (orc_e2m1_encode_nearest(f) != orc_e2m1_encode_binade(f)) {
+      if (!c->bad[tid]) c->first[tid] = c->start + (uint64_t)j;
+      ++c->bad[tid];
+    }
+  }
+}
+
+int64_t orc_e2m1_encoders_disagree(uint64_t start, uint64_t count, int nthreads, uint64_t *first_bad) {
+  e2m1_cmp *c = (e2m1_cmp *)calloc(1, sizeof(e2m1_cmp));
+  if (!c) return -1;
+  c->start = start;
+  int nt = resolve_threads(nthreads);
+  if (nt > E2M1_MAXT) nt = E2M1_MAXT;
+  parallel_for((int64_t)count, nt, e2m1_cmp_range, c);
+  int64_t bad = 0;
+  uint64_t first = 0;
+  for (int t = 0; t < E2M1_MAXT; ++t)
+    if (c->bad[t]) {
+      if (!bad || c->first[t] < first) first = c->first[t];
+      bad += c->bad[t];
+    }
+  free(c);
+  if (first_bad) *first_bad = first;
+  return bad;
+}
+
+/* Compare device-produced E2M1 codes (one per byte) of the fp32 patterns
+   start .. start+count-1 with the oracle encoder; NaN inputs are skipped. */
+typedef struct {
+  uint64_t start;
+  const uint8_t *codes;
+  int64_t bad[E2M1_MAXT];
+  uint64_t first[E2M1_MAXT];
+} e2m1_chk;
+
+static void e2m1_chk_range(void *p, int64_t lo, int64_t hi, int tid) {
+  e2m1_chk *c = (e2m1_chk *)p;
+  for (int64_t j = lo; j < hi; ++j) {
+    const uint32_t u = (uint32_t)(c->start + (uint64_t)j);
+    float f;
+    memcpy(&f, &u, 4);
+    if (isnan(f)) continue;
+    if ((c->codes[j] & 15u) != orc_e2m1_encode_nearest(f)) {
+      if (!c->bad[tid]) c->first[tid] = c->start + (uint64_t)j;
+      ++c->bad[tid];
+    }
+  }
+}
+
+int64_t orc_e2m1_check_codes(uint64_t start, uint64_t count, const uint8_t *codes, int nthreads,
+                             uint64_t *first_bad) {
+  e2m1_chk *c = (e2m1_chk *)calloc(1, sizeof(e2m1_chk));
+  if (!c) return -1;
+  c->start = start;
+  c->codes = codes;
+  int nt = resolve_threads(nthreads);
+  if (nt > E2M1_MAXT) nt = E2M1_MAXT;
+  parallel_for((int64_t)count, nt, e2m1_chk_range, c);
+  int64_t bad = 0;
+  uint64_t first = 0;
+  for (int t = 0; t < E2M1_MAXT; ++t)
+    if (c->bad[t]) {
+      if (!bad || c->first[t] < first) first = c->first[t];
+      bad += c->bad[t];
+    }
+  free(c);
+  if (first_bad) *first_bad = first;
+  return bad;
+}
+
+float orc_nvfp4_tensor_scale(float amax_t) {
+  float s = amax_t / 2688.0f; /* 6 * 448, exact in fp32 */
+  if (s == 0.0f || !isfinite(s)) s = 1.0f;
+  return s;
+}
+
+/* E4M3 code of the block microscale and the element multiplier S_inv. */
+static void nvfp4_block_scale(float amax_b, float s_t, uint8_t *code, float *s_b, float *s_inv) {
+  const float u = (amax_b / 6.0f) / s_t;
+  const uint8_t c = orc_encode_nearest(u, ORC_E4M3);
+  const float sb = (float)orc_decode(c, ORC_E4M3);
+  const float S = sb * s_t;
+  float si = 1.0f / S;
+  if (S == 0.0f || !isfinite(si)) si = 0.0f;
+  *code = c;
+  *s_b = sb;
+  *s_inv = si;
+}
+
+/* x: bf16 [rows x cols] (row stride ldx elements), cols % 16 == 0.
+   q: [rows x cols/2] bytes, element 2i in the low nibble of byte i.
+   sf: E4M3 codes, one per 16 elements: linear [rows][cols/16] or the tiled
+   128x4 layout of orc_mx_tiled_offset with cols/16 groups.
+   *tensor_scale: s_t (computed here from the tensor's amax when
+   static_tensor_scale is NULL, else taken from it). */
+int orc_quantize_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int sf_layout,
+                       const float *static_tensor_scale, uint8_t *q, uint8_t *sf, float *tensor_scale) {
+  if (rows < 0 || cols < 0 || cols % 16) return -1;
+  float amax_t = 0.0f;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const float v = fabsf(bf16_to_f32(x[r * ldx + c]));
+      if (v > amax_t || isnan(v)) amax_t = v;
+    }
+  const float s_t = static_tensor_scale ? *static_tensor_scale : orc_nvfp4_tensor_scale(amax_t);
+  *tensor_scale = s_t;
+  const int64_t ng = cols / 16;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t g = 0; g < ng; ++g) {
+      float amax_b = 0.0f;
+      for (int64_t i = 0; i < 16; ++i) {
+        const float v = fabsf(bf16_to_f32(x[r * ldx + g * 16 + i]));
+        if (v > amax_b) amax_b = v;
+      }
+      uint8_t code;
+      float sb, si;
+      nvfp4_block_scale(amax_b, s_t, &code, &sb, &si);
+      const int64_t off = sf_layout == ORC_SF_TILED ? orc_mx_tiled_offset(r, g, rows, ng) : r * ng + g;
+      sf[off] = code;
+      for (int64_t i = 0; i < 16; i += 2) {
+        const float a0 = bf16_to_f32(x[r * ldx + g * 16 + i]) * si;
+        const float a1 = bf16_to_f32(x[r * ldx + g * 16 + i + 1]) * si;
+        q[r * (cols / 2) + (g * 16 + i) / 2] =
+            (uint8_t)(orc_e2m1_encode_nearest(a0) | (orc_e2m1_encode_nearest(a1) << 4));
+      }
+    }
+  return 0;
+}
+
+static double nvfp4_value(const uint8_t *q, const uint8_t *sf, int sf_layout, float s_t, int64_t r, int64_t k,
+                          int64_t rows, int64_t cols) {
+  const uint8_t byte = q[r * (cols / 2) + k / 2];
+  const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
+  const int64_t ng = cols / 16;
+  const int64_t off = sf_layout == ORC_SF_TILED ? orc_mx_tiled_offset(r, k / 16, rows, ng) : r * ng + k / 16;
+  return orc_e2m1_decode(code) * orc_decode(sf[off], ORC_E4M3) * (double)s_t;
+}
+
+/* x_hat = bf16(fp32(decode(q) * fp32(s_b * s_t))). */
+int orc_dequantize_nvfp4(const uint8_t *q, const uint8_t *sf, int sf_layout, float s_t, int64_t rows, int64_t cols,
+                         uint16_t *out) {
+  if (rows < 0 || cols < 0 || cols % 16) return -1;
+  const int64_t ng = cols / 16;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t k = 0; k < cols; ++k) {
+      const uint8_t byte = q[r * (cols / 2) + k / 2];
+      const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
+      const int64_t off = sf_layout == ORC_SF_TILED ? orc_mx_tiled_offset(r, k / 16, rows, ng) : r * ng + k / 16;
+      const float S = (float)orc_decode(sf[off], ORC_E4M3) * s_t;
+      out[r * cols + k] = f32_to_bf16_rn((float)orc_e2m1_decode(code) * S);
+    }
+  return 0;
+}
+
+/* GEMM over NVFP4 operands: ref = sum_k x_hat * w_hat in double (every
+   product of an E2M1 value, an E4M3 microscale and an fp32 tensor scale is
+   exact in double), bound = sum_k |x_hat * w_hat|. rows / cols select
+   output entries (NULL = all). */
+int orc_gemm_nvfp4(const uint8_t *a, const uint8_t *sfa, float sta, const uint8_t *b, const uint8_t *sfb, float stb,
+                   int sf_layout, int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
+                   const int64_t *cols, int64_t ncols, double *ref, double *bound) {
+  if (M < 0 || N < 0 || K < 0 || K % 16) return -1;
+  if (!rows) nrows = M;
+  if (!cols) ncols = N;
+  double *xh = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+  double *wh = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)(ncols > 0 ? ncols : 1));
+  if (!xh || !wh) {
+    free(xh);
+    free(wh);
+    return -2;
+  }
+  for (int64_t j = 0; j < ncols; ++j) {
+    const int64_t n = cols ? cols[j] : j;
+    for (int64_t k = 0; k < K; ++k) wh[j * K + k] = nvfp4_value(b, sfb, sf_layout, stb, n, k, N, K);
+  }
+  for (int64_t i = 0; i < nrows; ++i) {
+    const int64_t m = rows ? rows[i] : i;
+    for (int64_t k = 0; k < K; ++k) xh[k] = nvfp4_value(a, sfa, sf_layout, sta, m, k, M, K);
+    for (int64_t j = 0; j < ncols; ++j) {
+      double acc = 0.0, bnd = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = xh[k] * wh[j * K + k];
+        acc += p;
+        bnd += fabs(p);
+      }
+      ref[i * ncols + j] = acc;
+      bound[i * ncols + j] = bnd;
+    }
+  }
+  free(xh);
+  free(wh);
+  return 0;
+}

@@ -1,0 +1,136 @@
+"""GPU parity of the NVFP4 path ("Low precision: FP8, FP4, and microscaling",
+NVFP4 paragraph) against the CPU oracle.
+
+Quantizer, dequantizer and the element conversion: bit-exact (codes, E4M3
+block scales, tensor scale, bf16 output). GEMM: |gpu - ref| <= 1e-3 * bound +
+half a bf16 ulp of ref (the same rule as the FP8 GEMMs), and exact for small
+values with power-of-two scales.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_04_gb300 import binding as fb
+from fp8_block_scaled_04_gb300 import synth
+from gpu_util import out_f64, to_dev_bf16, within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+def test_e2m1_encode_every_fp32():
+    """The quantizer's element step against the oracle encoder on all 2^32 fp32 patterns."""
+    chunk = 1 << 28
+    for start in range(0, 1 << 32, chunk):
+        bits = torch.arange(start, start + chunk, dtype=torch.int64, device="cuda").to(torch.int32)
+        codes = fb.debug_encode_e2m1_f32(bits.view(torch.float32))
+        bad, first = oracle.e2m1_check_codes(start, codes.cpu().numpy())
+        assert bad == 0, "first mismatch at fp32 pattern 0x%08x" % first
+
+
+def _quant_dev(x, layout, static=None):
+    q, sf, ts = fb.quantize_nvfp4(to_dev_bf16(x), layout,
+                                  None if static is None else torch.tensor([static], dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), sf.cpu().numpy(), float(ts.item())
+
+
+@pytest.mark.parametrize("layout", [fb.SF_LINEAR, fb.SF_TCGEN05])
+@pytest.mark.parametrize("shape", [(1, 16), (7, 48), (130, 272), (257, 1024), (300, 4096), (2048, 7168)])
+def test_quantize_bit_exact(shape, layout):
+    rows, cols = shape
+    x = synth.bf16_matrix(rows, cols, 1.0, 900 + rows, 901 + cols, 0.01, 40.0)
+    q, sf, ts = _quant_dev(x, layout)
+    qo, sfo, tso = oracle.quantize_nvfp4(x, layout)
+    assert np.float32(ts) == np.float32(tso)
+    assert np.array_equal(q, qo)
+    assert np.array_equal(sf[: sfo.size], sfo)
+
+
+def test_quantize_static_scale_and_extremes():
+    rows, cols = 64, 512
+    x = synth.bf16_matrix(rows, cols, 1.0, 911, 912, 0.02, 50.0)
+    x[3, :] = 0                        # all-zero blocks
+    x[5, 16:32] = 0x0001               # smallest bf16 subnormals
+    x[6, 32:48] = 0x7F7F               # largest finite bf16
+    x[7, 0:16] = 0x8000                # negative zeros
+    for static in [None, 0.01, 3.0e-3]:
+        q, sf, ts = _quant_dev(x, fb.SF_TCGEN05, static)
+        qo, sfo, tso = oracle.quantize_nvfp4(x, fb.SF_TCGEN05, static)
+        assert np.float32(ts) == np.float32(tso)
+        assert np.array_equal(q, qo), static
+        assert np.array_equal(sf, sfo), static
+
+
+@pytest.mark.parametrize("layout", [fb.SF_LINEAR, fb.SF_TCGEN05])
+def test_dequantize_bit_exact(layout):
+    rows, cols = 130, 1024
+    x = synth.bf16_matrix(rows, cols, 1.0, 921, 922, 0.01, 40.0)
+    qo, sfo, tso = oracle.quantize_nvfp4(x, layout)
+    out = fb.dequantize_nvfp4(torch.from_numpy(qo).cuda(), torch.from_numpy(sfo).cuda(),
+                              torch.tensor([tso], dtype=torch.float32, device="cuda"), cols, layout)
+    torch.cuda.synchronize()
+    ref = oracle.dequantize_nvfp4(qo, sfo, tso, cols, layout)
+    assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+def _gemm_dev(qa, sfa, ta, qb, sfb, tb):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    f = lambda v: torch.tensor([v], dtype=torch.float32, device="cuda")
+    out = fb.gemm_nvfp4(torch.from_numpy(qa).cuda(), torch.from_numpy(sfa).cuda(), f(ta),
+                        torch.from_numpy(qb).cuda(), torch.from_numpy(sfb).cuda(), f(tb), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (130, 272, 512), (1, 16, 256), (300, 640, 1024),
+                                   (257, 512, 2048)])
+def test_gemm_parity(M, N, K):
+    x = synth.bf16_matrix(M, K, 1.0, 930 + M, 931 + K, 0.01, 40.0)
+    w = synth.bf16_matrix(N, K, 1.0, 932 + N, 933 + K, 0.01, 40.0)
+    qa, sfa, ta = oracle.quantize_nvfp4(x, oracle.SF_TILED)
+    qb, sfb, tb = oracle.quantize_nvfp4(w, oracle.SF_TILED)
+    out = _gemm_dev(qa, sfa, ta, qb, sfb, tb)
+    ref, bound = oracle.gemm_nvfp4(qa, sfa, ta, qb, sfb, tb, oracle.SF_TILED)
+    bad, worst = within_tolerance(out_f64(out), ref, bound)
+    assert bad == 0, (bad, worst)
+
+
+def test_gemm_small_values_exact():
+    """E2M1 codes with power-of-two microscales and tensor scales, K <= 512: fp32 sums are exact."""
+    rng = np.random.default_rng(17)
+    M, N, K = 130, 272, 512
+
+    def operand(rows):
+        c = rng.integers(0, 16, (rows, K)).astype(np.uint8)
+        q = (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+        sf = np.zeros(oracle.mx_tiled_bytes(rows, K // 16), np.uint8)
+        for r in range(rows):
+            for g in range(K // 16):
+                sf[oracle.mx_tiled_offset(r, g, rows, K // 16)] = [0x30, 0x38, 0x40][(r + g) % 3]  # 0.5, 1, 2
+        return q, sf
+
+    qa, sfa = operand(M)
+    qb, sfb = operand(N)
+    out = _gemm_dev(qa, sfa, 0.5, qb, sfb, 2.0)
+    ref, _ = oracle.gemm_nvfp4(qa, sfa, 0.5, qb, sfb, 2.0, oracle.SF_TILED)
+    expect = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(out_f64(out), expect)
+
+
+def test_gemm_quantized_by_the_gpu_prefill_shape_sampled():
+    """GPU quantizer feeding the GPU GEMM at 4096 x 14336 x 4096, sampled rows against the oracle."""
+    M, N, K = 4096, 14336, 4096
+    x = synth.bf16_matrix(M, K, 1.0, 940, 941, 0.01, 30.0)
+    w = synth.bf16_matrix(N, K, 0.02, 942)
+    qa, sfa, ta = fb.quantize_nvfp4(to_dev_bf16(x))
+    qb, sfb, tb = fb.quantize_nvfp4(to_dev_bf16(w))
+    out = fb.gemm_nvfp4(qa, sfa, ta, qb, sfb, tb)
+    torch.cuda.synchronize()
+    qa_h, sfa_h, ta_h = qa.cpu().numpy(), sfa.cpu().numpy(), float(ta.item())
+    qb_h, sfb_h, tb_h = qb.cpu().numpy(), sfb.cpu().numpy(), float(tb.item())
+    rows = np.unique(np.concatenate([np.arange(0, M, 509), [M - 1]]))
+    ref, bound = oracle.gemm_nvfp4(qa_h, sfa_h, ta_h, qb_h, sfb_h, tb_h, oracle.SF_TILED, rows=rows)
+    bad, worst = within_tolerance(out_f64(out)[rows], ref, bound)
+    assert bad == 0, (bad, worst)
