@@ -91,6 +91,12 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
 #ifndef FOLD_WIDE_STAGES
 #define FOLD_WIDE_STAGES 4  // stages of the 128 x 256 fold kernel (3 leaves room for two epilogue slots per warp)
 #endif
+#ifndef NVF4_COPIERS
+#define NVF4_COPIERS 2  // scale-copier warps of the NVFP4 GEMM (12 atom copies per k-block)
+#endif
+#ifndef SF_COPIER
+#define SF_COPIER 1  // block-scaled GEMMs: a separate warp copies scale atoms to tensor memory
+#endif
 #ifndef FOLD_USE_PAIRS
 #define FOLD_USE_PAIRS 0  // 1: block-scaled GEMMs with M > 128 run on CTA pairs (measured slower)
 #endif
@@ -1156,13 +1162,48 @@ struct AccCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
   static constexpr int CONSUMER_WARPS = 4 * (BN / 128);
-  static constexpr int THREADS = 64 + 32 * CONSUMER_WARPS;
+  // warp 0 producer, warp 1 MMA issuer, (block-scaled kinds) warp 2 copies the
+  // stage's scale atoms into tensor memory, then the epilogue warps
+  static constexpr bool COPIER = MX && SF_COPIER;
+  // copier warps: the stage's atoms are split round-robin between them
+  static constexpr int COPIERS = !COPIER ? 0 : (KIND == KIND_NVF4 ? NVF4_COPIERS : 1);
+  static constexpr int FIRST_CONSUMER_WARP = 2 + COPIERS;
+  static constexpr int THREADS = 32 * FIRST_CONSUMER_WARP + 32 * CONSUMER_WARPS;
   static constexpr int SF_COLS = 4 * ATOMS * (1 + BN / 128);  // tensor-memory columns per stage
   static constexpr int ACC_COLS = NACC * BN;                    // NACC accumulators (2: epilogue overlaps MMA)
   static constexpr uint32_t TMEM_COLS = ACC_COLS + STAGES * SF_COLS <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_STRIDE + 1024;
   static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory budget");
 };
+
+// A stage's scale atoms, shared memory (sf_smem: A's atoms, then B's per
+// 128-row block) -> tensor memory (sf_tmem). MXFP8: one atom per 128 rows at
+// +4 columns per block. NVFP4: four atoms per 128 rows; A's atom k at +4k, B's
+// at +8k (+4 for the second 128-row block).
+// With several copiers, copier `part` of `nparts` issues the atoms whose index
+// (in the order below) is congruent to part.
+template <int KIND, int BN>
+__device__ __forceinline__ void copy_scale_atoms(uint32_t sf_tmem, uint32_t sf_smem, int part = 0, int nparts = 1) {
+  if constexpr (KIND == KIND_NVF4) {
+    constexpr int PER_K = 1 + BN / 128;  // A's atom, then B's per 128-row block
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if ((k * PER_K) % nparts == part)
+        tmem_cp_32x128b_warpx4(sf_tmem + 4 * k, sdesc_plain_32x16(sf_smem + 512 * k));
+#pragma unroll
+      for (int j = 0; j < BN / 128; ++j)
+        if ((k * PER_K + 1 + j) % nparts == part)
+          tmem_cp_32x128b_warpx4(sf_tmem + 16 + 8 * k + 4 * j,
+                                 sdesc_plain_32x16(sf_smem + 2048 + 2048 * j + 512 * k));
+    }
+  } else {
+    if (part == 0) tmem_cp_32x128b_warpx4(sf_tmem, sdesc_plain_32x16(sf_smem));
+#pragma unroll
+    for (int j = 0; j < BN / 128; ++j)
+      if ((1 + j) % nparts == part)
+        tmem_cp_32x128b_warpx4(sf_tmem + 4 + 4 * j, sdesc_plain_32x16(sf_smem + 512 + 512 * j));
+  }
+}
 
 template <int KIND, int BN, int STAGES, int NACC>
 __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
@@ -1175,7 +1216,8 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
   constexpr bool F4 = KIND == KIND_NVF4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  __shared__ uint64_t full[STAGES], empty[STAGES], afull[NACC], aempty[NACC], drain;
+  // sf_ready[s]: the scale atoms of stage s are in tensor memory (copier warp)
+  __shared__ uint64_t full[STAGES], empty[STAGES], sf_ready[STAGES], afull[NACC], aempty[NACC], drain, cdrain;
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -1190,12 +1232,14 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], C::COPIERS > 0 ? C::COPIERS : 1);
     }
     for (int b = 0; b < NACC; ++b) {
       mbar_init(&afull[b], 1);
       mbar_init(&aempty[b], C::CONSUMER_WARPS);
     }
     mbar_init(&drain, 1);
+    mbar_init(&cdrain, C::COPIERS > 0 ? C::COPIERS : 1);  // every copier's copies are done
     ctl.abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -1248,6 +1292,32 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
         drain_stages<STAGES>(full, it);
       }
     }
+  } else if (C::COPIER && warp >= 2 && warp < C::FIRST_CONSUMER_WARP) {
+    // scale-factor copiers: stage s's atoms smem -> tensor memory once its
+    // copies have landed; the slot's previous MMA is done (the producer waited
+    // on it before loading the stage)
+    if (lane == 0) {
+      const int part = warp - 2;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          copy_scale_atoms<KIND, BN>(tmem + static_cast<uint32_t>(C::ACC_COLS + s * C::SF_COLS),
+                                     smem_u32(smem + s * C::STAGE_STRIDE) + C::A_BYTES + C::B_BYTES, part,
+                                     C::COPIERS);
+          tc_commit(&sf_ready[s]);
+        }
+      }
+      if (!ok) flag_abort(&ctl, dev_status);
+      tc_commit(&cdrain);
+      mbar_wait(&cdrain, 0, kDrainTimeoutNs, nullptr);
+    }
   } else if (warp == 1) {
     if (lane == 0) {
       int it = 0, tc = 0;
@@ -1263,28 +1333,22 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
         const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
-          if (!mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+          // with a copier warp, sf_ready[s] implies full[s]
+          if (!mbar_wait(C::COPIER ? &sf_ready[s] : &full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + s * C::STAGE_STRIDE);
           const uint32_t b0 = a0 + C::A_BYTES;
+          if constexpr (MX && !C::COPIER)
+            copy_scale_atoms<KIND, BN>(tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS), b0 + C::B_BYTES);
           if (F4) {
             // NVFP4: one scale atom per MMA (K = 64, four 16-element scales per
             // row); A's atom k at column +4k, B's at +8k (second 128-row block
             // of B at +4, as the block-scaled MMA reads a 256-row B)
             const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + 16;
-            const uint32_t sf_smem = b0 + C::B_BYTES;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              tmem_cp_32x128b_warpx4(sfa_t + 4 * k, sdesc_plain_32x16(sf_smem + 512 * k));
-#pragma unroll
-              for (int j = 0; j < BN / 128; ++j)
-                tmem_cp_32x128b_warpx4(sfb_t + 8 * k + 4 * j,
-                                       sdesc_plain_32x16(sf_smem + 2048 + 2048 * j + 512 * k));
-            }
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_mxf4nvf4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, sfa_t + 4 * k,
@@ -1292,11 +1356,6 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
           } else if (MX) {
             const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + 4;
-            const uint32_t sf_smem = b0 + C::B_BYTES;
-            tmem_cp_32x128b_warpx4(sfa_t, sdesc_plain_32x16(sf_smem));
-#pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tmem_cp_32x128b_warpx4(sfb_t + 4 * j, sdesc_plain_32x16(sf_smem + 512 + 512 * j));
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k)
               mma_mxf8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k),
@@ -1319,7 +1378,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------ epilogue consumers
-    const int cw = warp - 2;
+    const int cw = warp - C::FIRST_CONSUMER_WARP;
     const int quarter = warp & 3;
     const int half = cw >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
