@@ -428,6 +428,46 @@ def measure_mx(args, fb, synth, dev, stream, flush, fp8_peak):
                              "frac_nominal_4.5PF": round(tf / 4500.0, 4)}}
 
 
+def measure_nvfp4(args, fb, synth, dev, stream, flush, hbm_peak, fp4_peak):
+    """NVFP4 ("Low precision", NVFP4 paragraph): the quantizer on the sweep tensor
+    16384 x 8192 (two passes with the tensor's own amax, and one pass with a
+    static tensor scale) and the block-scaled GEMM 8192^3 on the MX inputs."""
+    import numpy as np
+    import torch
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    reps = max(10, args.steps)
+    res = {}
+    R, C = 16384, 8192
+    x = to_dev(synth.sweep_x(R, C))
+    q, sf, ts = fb.quantize_nvfp4(x)
+    out_bytes = R * C // 2 + R * C // 16
+    t2 = _time_kernel(lambda: fb.quantize_nvfp4(x, q=q, sf=sf, tensor_scale=ts), flush, stream, reps)
+    b2 = 2 * (2 * R * C) + out_bytes  # amax pass reads X, the encode pass reads it again
+    static = torch.tensor([0.01], dtype=torch.float32, device=dev)
+    t1 = _time_kernel(lambda: fb.quantize_nvfp4(x, static_tensor_scale=static, q=q, sf=sf, tensor_scale=ts),
+                      flush, stream, reps)
+    b1 = 2 * R * C + out_bytes
+    res["nvfp4_quantize_16384x8192"] = {
+        "two_pass": {"ms": round(t2, 5), "GB/s": round(b2 / (t2 * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(b2 / (t2 * 1e-3) / 1e9 / hbm_peak, 4), "algorithmic_bytes": b2},
+        "static_scale": {"ms": round(t1, 5), "GB/s": round(b1 / (t1 * 1e-3) / 1e9, 1),
+                         "frac_hbm": round(b1 / (t1 * 1e-3) / 1e9 / hbm_peak, 4), "algorithmic_bytes": b1}}
+    del x, q, sf
+    S = 8192
+    qa, sfa, ta = fb.quantize_nvfp4(to_dev(synth.mx_x(S, S)))
+    qb, sfb, tb = fb.quantize_nvfp4(to_dev(synth.mx_w(S, S)))
+    o = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
+    t = _time_kernel(lambda: fb.gemm_nvfp4(qa, sfa, ta, qb, sfb, tb, out=o), flush, stream, reps)
+    tf = 2.0 * S ** 3 / (t * 1e-3) / 1e12
+    res["nvfp4_gemm_8192"] = {"ms": round(t, 5), "TFLOP/s": round(tf, 1), "frac_fp4_peak": round(tf / fp4_peak, 4),
+                              "fp4_peak_src": "measured bf16 burst x 6 (fp4/bf16 nominal ratio 13.5/2.25)",
+                              "frac_nominal_13.5PF": round(tf / 13500.0, 4)}
+    return res
+
+
 def run_workload(args):
     """One non-headline workload on its own (for profiling): prints one JSON line."""
     import torch
@@ -444,6 +484,8 @@ def run_workload(args):
         res = {"quantize_sweep_16384x8192": measure_sweep(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"])}
     elif args.workload == "decode":
         res = measure_decode(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"])
+    elif args.workload == "nvfp4":
+        res = measure_nvfp4(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"], 6.0 * peaks["bf16_tflops"])
     else:
         res = measure_mx(args, fb, synth, dev, stream, flush, 2.0 * peaks["bf16_tflops"])
     print(json.dumps({"workload": args.workload, "peaks": peaks["src"], "results": res}))
@@ -454,6 +496,7 @@ def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_p
     res = {"quantize_sweep_16384x8192": measure_sweep(args, fb, synth, dev, stream, flush, hbm_peak)}
     res.update(measure_decode(args, fb, synth, dev, stream, flush, hbm_peak))
     res.update(measure_mx(args, fb, synth, dev, stream, flush, fp8_peak))
+    res.update(measure_nvfp4(args, fb, synth, dev, stream, flush, hbm_peak, 3.0 * fp8_peak))
     return res
 
 
@@ -529,7 +572,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--headline-only", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "sweep", "decode", "mx"],
+    ap.add_argument("--workload", default="all", choices=["all", "sweep", "decode", "mx", "nvfp4"],
                     help="all: the headline step plus the other workloads; otherwise that workload alone")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()

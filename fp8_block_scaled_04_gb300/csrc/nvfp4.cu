@@ -74,7 +74,40 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t g, int64_t ng, b
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
-// One lane per 16-element block; a warp covers 32 consecutive blocks of a row.
+// Streaming 16-byte load that does not allocate in L1 (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// One 16-element block: its E4M3 scale code and the eight packed code bytes.
+__device__ __forceinline__ void encode_block(const uint4 v0, const uint4 v1, float s_t, uint32_t &code, uint2 &packed) {
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+  const float amax_b = bf16_bits_to_f32(m);
+  const float u = __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_t);
+  code = e4m3_code(u);
+  const float S = __fmul_rn(e4m3_value(code), s_t);
+  float s_inv = __frcp_rn(S);
+  if (S == 0.0f || !isfinite(s_inv)) s_inv = 0.0f;
+  float lo[8], hi[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    lo[2 * i] = __fmul_rn(bf16_bits_to_f32(w[i] & 0xffffu), s_inv);
+    lo[2 * i + 1] = __fmul_rn(bf16_bits_to_f32(w[i] >> 16), s_inv);
+    hi[2 * i] = __fmul_rn(bf16_bits_to_f32(w[4 + i] & 0xffffu), s_inv);
+    hi[2 * i + 1] = __fmul_rn(bf16_bits_to_f32(w[4 + i] >> 16), s_inv);
+  }
+  packed = make_uint2(e2m1x8(lo), e2m1x8(hi));
+}
+
+// A warp covers 64 consecutive blocks of a row per task: lane l takes blocks
+// l and l + 32 (all four 16-byte loads in flight before any arithmetic).
 // amax_bits: the tensor's amax (fp32 bits) from the amax pass, or nullptr when
 // static_ts gives the tensor scale.
 __global__ void __launch_bounds__(kThreads)
@@ -86,36 +119,31 @@ __global__ void __launch_bounds__(kThreads)
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = s_t;
   const int lane = threadIdx.x & 31;
   const int64_t ng = cols / 16;
-  const int64_t chunks = (ng + 31) / 32;
+  const int64_t chunks = (ng + 63) / 64;
   const int64_t tasks = rows * chunks;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
   for (int64_t t = warp0; t < tasks; t += nwarps) {
     const int64_t r = t / chunks;
-    const int64_t g = (t - r * chunks) * 32 + lane;
-    if (g >= ng) continue;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + g * 16);
-    const uint4 v0 = src[0], v1 = src[1];
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
-    const float amax_b = bf16_bits_to_f32(m);
-    const float u = __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_t);
-    const uint32_t code = e4m3_code(u);
-    const float S = __fmul_rn(e4m3_value(code), s_t);
-    float s_inv = __frcp_rn(S);
-    if (S == 0.0f || !isfinite(s_inv)) s_inv = 0.0f;
-    float lo[8], hi[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      lo[2 * i] = __fmul_rn(bf16_bits_to_f32(w[i] & 0xffffu), s_inv);
-      lo[2 * i + 1] = __fmul_rn(bf16_bits_to_f32(w[i] >> 16), s_inv);
-      hi[2 * i] = __fmul_rn(bf16_bits_to_f32(w[4 + i] & 0xffffu), s_inv);
-      hi[2 * i + 1] = __fmul_rn(bf16_bits_to_f32(w[4 + i] >> 16), s_inv);
+    const int64_t g0 = (t - r * chunks) * 64 + lane, g1 = g0 + 32;
+    const uint16_t *row = x + r * ldx;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint4 a0 = g0 < ng ? ld_stream16(row + g0 * 16) : zero;
+    const uint4 a1 = g0 < ng ? ld_stream16(row + g0 * 16 + 8) : zero;
+    const uint4 b0 = g1 < ng ? ld_stream16(row + g1 * 16) : zero;
+    const uint4 b1 = g1 < ng ? ld_stream16(row + g1 * 16 + 8) : zero;
+    uint32_t c0, c1;
+    uint2 p0, p1;
+    encode_block(a0, a1, s_t, c0, p0);
+    encode_block(b0, b1, s_t, c1, p1);
+    if (g0 < ng) {
+      *reinterpret_cast<uint2 *>(q + r * ldq + g0 * 8) = p0;
+      sf[sf_offset(r, g0, ng, tiled)] = static_cast<uint8_t>(c0);
     }
-    *reinterpret_cast<uint2 *>(q + r * ldq + g * 8) = make_uint2(e2m1x8(lo), e2m1x8(hi));
-    sf[sf_offset(r, g, ng, tiled)] = static_cast<uint8_t>(code);
+    if (g1 < ng) {
+      *reinterpret_cast<uint2 *>(q + r * ldq + g1 * 8) = p1;
+      sf[sf_offset(r, g1, ng, tiled)] = static_cast<uint8_t>(c1);
+    }
   }
 }
 
@@ -182,7 +210,7 @@ int grid_for(int64_t work_items) {
 fp8_status_t launch_quantize_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, bool tiled,
                                    const float *static_ts, uint8_t *q, int64_t ld_q, uint8_t *sf, float *ts_out,
                                    uint32_t *amax_ws, cudaStream_t stream) {
-  const int64_t tasks = rows * ((cols / 16 + 31) / 32);
+  const int64_t tasks = rows * ((cols / 16 + 63) / 64);
   if (static_ts == nullptr) {
     if (cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
     if (launch_amax(x, rows, cols, ld_x, amax_ws, stream) != FP8_OK) return FP8_ERR_CUDA;
