@@ -64,6 +64,8 @@ def lib():
         L.fp8_dequantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp]
         L.fp8_gemm_nvfp4.restype = i32
         L.fp8_gemm_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+        L.fp8_debug_gemm_blockscaled_pairs.restype = i32
+        L.fp8_debug_gemm_blockscaled_pairs.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
         L.fp8_debug_encode_e2m1_f32.restype = i32
         L.fp8_debug_encode_e2m1_f32.argtypes = [vp, i64, vp, vp]
         L.fp8_debug_encode_f32.restype = i32
@@ -294,6 +296,21 @@ def debug_encode_f32(x, fmt: int, out=None, stream=None):
     if out is None:
         out = torch.empty(x.numel(), dtype=torch.uint8, device=x.device)
     _check(lib().fp8_debug_encode_f32(_ptr(x), x.numel(), fmt, _ptr(out), _stream(stream)), "fp8_debug_encode_f32")
+    return out
+
+
+def debug_gemm_blockscaled_pairs(a, a_scales, b, b_scales, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None,
+                                 status=None, stream=None):
+    """The 1x128 x 128x128 block-scaled GEMM on the CTA-pair kernel, whatever the shape."""
+    import torch
+
+    M, K = a.shape
+    N = b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    rc = lib().fp8_debug_gemm_blockscaled_pairs(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), a_fmt, b_fmt,
+                                                _ptr(out), M, N, K, _ptr(status), _stream(stream))
+    _check(rc, "fp8_debug_gemm_blockscaled_pairs")
     return out
 
 

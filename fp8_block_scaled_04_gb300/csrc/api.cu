@@ -365,6 +365,22 @@ fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fm
   return launch_encode_f32(x_dev, n, fmt, static_cast<uint8_t *>(out_dev), reinterpret_cast<cudaStream_t>(stream));
 }
 
+fp8_status_t fp8_debug_gemm_blockscaled_pairs(const void *a_dev, const float *a_scales_dev, const void *b_dev,
+                                              const float *b_scales_dev, fp8_format_t a_fmt, fp8_format_t b_fmt,
+                                              void *out_dev, int64_t M, int64_t N, int64_t K, int *dev_status,
+                                              fp8_stream_t stream) {
+  fp8_status_t st = check_gemm_common(a_dev, b_dev, out_dev, M, N, K, a_fmt, b_fmt);
+  if (st != FP8_OK || M == 0 || N == 0) return st;
+  if (K % 128 != 0) return FP8_ERR_UNSUPPORTED_SHAPE;
+  if (a_scales_dev == nullptr || b_scales_dev == nullptr) return FP8_ERR_INVALID_ARG;
+  if (!aligned(a_scales_dev, 4) || !aligned(b_scales_dev, 4)) return FP8_ERR_ALIGNMENT;
+  if (dev_status != nullptr && !aligned(dev_status, 4)) return FP8_ERR_ALIGNMENT;
+  return launch_gemm_fold_pairs(static_cast<const uint8_t *>(a_dev), a_scales_dev,
+                                static_cast<const uint8_t *>(b_dev), b_scales_dev, a_fmt, b_fmt,
+                                static_cast<uint16_t *>(out_dev), M, N, K, dev_status,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
 fp8_status_t fp8_debug_encode_e2m1_f32(const float *x_dev, int64_t n, void *out_dev, fp8_stream_t stream) {
   if (n < 0 || n % 8) return FP8_ERR_INVALID_ARG;
   if (n == 0) return FP8_OK;

@@ -1674,6 +1674,13 @@ fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *
   return launch_fold_tiles<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
 }
 
+// The CTA-pair fold kernel regardless of the shape rule (M >= 1): for its tests.
+fp8_status_t launch_gemm_fold_pairs(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
+                                    int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
+                                    cudaStream_t stream) {
+  return launch_fold_pairs<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
+}
+
 fp8_status_t launch_gemm_fold_quantized(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
                                         int a_fmt, int b_fmt, int out_fmt, uint8_t *q_out, float *q_scales,
                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {

@@ -291,6 +291,17 @@ fp8_status_t fp8_gemm_nvfp4(const void *a_dev, const void *a_sf_dev, const float
 fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fmt, void *out_dev,
                                   fp8_stream_t stream);
 
+/* fp8_gemm_blockscaled with 1x128 / 128x128 scales on the CTA-pair kernel
+ * (tcgen05 cta_group::2, 256 x 256 tiles over a cluster of two CTAs) whatever
+ * the shape: the kernel the library keeps for shapes it may suit but does not
+ * select by default (it measured 3-5 % slower than the single-CTA kernel on the
+ * prefill shapes). Same arguments and rules as fp8_gemm_blockscaled with
+ * a_gran = TILE_1x128, b_gran = BLOCK_128x128. */
+fp8_status_t fp8_debug_gemm_blockscaled_pairs(const void *a_dev, const float *a_scales_dev, const void *b_dev,
+                                              const float *b_scales_dev, fp8_format_t a_fmt, fp8_format_t b_fmt,
+                                              void *out_dev, int64_t M, int64_t N, int64_t K, int *dev_status,
+                                              fp8_stream_t stream);
+
 /* Codec check for NVFP4's element step (same role as fp8_debug_encode_f32):
  * out[i] = the E2M1 code (low 4 bits of byte i) of x[i], rounded to nearest
  * even and saturated at +-6 by the device routine fp8_quantize_nvfp4 uses.

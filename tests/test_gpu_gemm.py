@@ -62,14 +62,19 @@ def test_fold_ragged_shapes(M, N, K):
     assert bad == 0, (bad, worst)
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 2560, 256), (2000, 2480, 384), (4096, 2432, 640)])
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 256), (2000, 2480, 384), (4096, 2432, 640), (130, 272, 512),
+                                   (1, 16, 128)])
 def test_fold_on_cta_pairs(M, N, K):
-    """Shapes with enough 256 x 256 tiles for the CTA-pair kernel (ragged in M and N)."""
+    """The CTA-pair kernel (cta_group::2, 256 x 256 tiles) on ragged shapes, small ones included."""
     x = synth.bf16_matrix(M, K, 1.0, 60 + M, 61 + K, 0.01, 50.0)
     w = synth.bf16_matrix(N, K, 0.02, 62 + N)
     qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
-    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
-    rows = np.unique(np.concatenate([np.arange(0, M, 97), np.arange(M - 130, M), np.arange(120, 390)]))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = fb.debug_gemm_blockscaled_pairs(torch.from_numpy(qa).cuda(), torch.from_numpy(sa).cuda(),
+                                          torch.from_numpy(qb).cuda(), torch.from_numpy(sb).cuda(), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), np.arange(max(0, M - 130), M), np.arange(min(120, M), min(390, M))]))
     ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, rows=rows)
     bad, worst = within_tolerance(out_f64(out)[rows], ref, bound)
     assert bad == 0, (bad, worst)
