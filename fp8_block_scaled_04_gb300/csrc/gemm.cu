@@ -306,6 +306,9 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // setup above overlaps the previous kernel (dependent launch); its outputs
+  // (the operands and scales) are read only after this
+  grid_dependency_wait();
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp < C::FIRST_CONSUMER_WARP) {
@@ -1615,6 +1618,25 @@ fp8_status_t launch_fold_pairs(const uint8_t *a, const float *sa, const uint8_t 
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// Launch with programmatic stream serialization: the kernel may begin (and do
+// its setup) while the previous kernel in the stream finishes; it waits for
+// that kernel's results with grid_dependency_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // CTA pairs need at least 256 rows and enough pair tiles to fill the GPU.
 bool use_pairs(int64_t M, int64_t N) {
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
@@ -1641,9 +1663,10 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
     auto kern = gemm_fold_kernel<BN, ST, QFMT>;
     if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
     const int ntiles = static_cast<int>(tiles256);
-    kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-        ta, tb, to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
+    if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, ta, tb,
+                         to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K)) != cudaSuccess)
+      return FP8_ERR_CUDA;
   } else {
     constexpr int BN = 128, ST = 6;
     using C = FoldCfg<BN, ST>;
@@ -1651,9 +1674,10 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
     auto kern = gemm_fold_kernel<BN, ST, QFMT>;
     if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
     const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + 127) / 128));
-    kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-        ta, tb, to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-        idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
+    if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, ta, tb,
+                         to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K)) != cudaSuccess)
+      return FP8_ERR_CUDA;
   }
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;

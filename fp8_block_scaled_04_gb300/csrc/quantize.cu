@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
   constexpr int GPS = 32 / TPG;             // groups per slot (2 for 1x128, 8 for MX)
   constexpr int PAIRS = kVecPerLane * GPS;  // (slot, group) pairs per task: 8 or 32
   static_assert(PAIRS <= 32, "one pair per lane");
+  grid_dependents_launch();  // a GEMM launched after this may set itself up meanwhile
   const int lane = threadIdx.x & 31;
   const int64_t vec_per_row = cols >> 3;
   const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
