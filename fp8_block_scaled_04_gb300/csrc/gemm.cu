@@ -880,10 +880,15 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
+        // lane l forms s_w * s_x for activation rows l (+ 32 r) once; the
+        // shuffles then carry finished products (same fp32 multiply)
+        float cs[XR];
+#pragma unroll
+        for (int q = 0; q < XR; ++q) cs[q] = w0 * x0[q];
 #pragma unroll
         for (int j = 0; j < BX; ++j) {
-          const float sx = __shfl_sync(0xffffffffu, x0[j / 32], j % 32);
-          acc[j] = fmaf(w0 * sx, __uint_as_float(r[j]), acc[j]);
+          const float sc = __shfl_sync(0xffffffffu, cs[j / 32], j % 32);
+          acc[j] = fmaf(sc, __uint_as_float(r[j]), acc[j]);
         }
 #pragma unroll
         for (int r = 0; r < XR; ++r) {
@@ -1085,10 +1090,15 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
+        // lane l forms s_w * s_x for activation rows l (+ 32 r) once; the
+        // shuffles then carry finished products (same fp32 multiply)
+        float cs[XR];
+#pragma unroll
+        for (int q = 0; q < XR; ++q) cs[q] = w0 * x0[q];
 #pragma unroll
         for (int j = 0; j < BX; ++j) {
-          const float sx = __shfl_sync(0xffffffffu, x0[j / 32], j % 32);
-          acc[j] = fmaf(w0 * sx, __uint_as_float(r[j]), acc[j]);
+          const float sc = __shfl_sync(0xffffffffu, cs[j / 32], j % 32);
+          acc[j] = fmaf(sc, __uint_as_float(r[j]), acc[j]);
         }
 #pragma unroll
         for (int r = 0; r < XR; ++r) {
