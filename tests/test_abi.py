@@ -143,6 +143,63 @@ def test_gemm_refusals(L):
     assert fb.launch_count() == n0
 
 
+def test_nvfp4_scales_bytes(L):
+    # linear: one byte per 16 elements; tiled: 512-byte atoms of 128 rows x 4 groups, padded
+    assert fb.nvfp4_scales_bytes(130, 272, fb.SF_LINEAR) == 130 * 17
+    assert fb.nvfp4_scales_bytes(130, 272, fb.SF_TCGEN05) == 2 * 5 * 512
+    assert fb.nvfp4_scales_bytes(128, 64, fb.SF_TCGEN05) == 512
+    for rows, cols in [(1, 16), (257, 1024), (300, 4096)]:
+        assert fb.nvfp4_scales_bytes(rows, cols, fb.SF_TCGEN05) == oracle.mx_tiled_bytes(rows, cols // 16)
+    assert fb.nvfp4_scales_bytes(4, 40, fb.SF_LINEAR) == 0   # cols % 16
+    assert fb.nvfp4_scales_bytes(-1, 16, fb.SF_LINEAR) == 0
+    assert fb.nvfp4_scales_bytes(4, 16, 7) == 0
+
+
+def _q4(L, x=A16, rows=8, cols=128, ldx=128, lay=1, st=None, q=A16b, ldq=64, sf=A16, ts=A16, ws=A16, wsb=256):
+    return L.fp8_quantize_nvfp4(x, rows, cols, ldx, lay, st, q, ldq, sf, ts, ws, wsb, None)
+
+
+def test_nvfp4_refusals(L):
+    n0 = fb.launch_count()
+    assert _q4(L, rows=0) == fb.OK
+    assert _q4(L, lay=5) == fb.ERR_INVALID_ARG
+    assert _q4(L, cols=120, ldx=128) == fb.ERR_UNSUPPORTED_SHAPE  # % 16
+    assert _q4(L, x=None) == fb.ERR_INVALID_ARG
+    assert _q4(L, sf=None) == fb.ERR_INVALID_ARG
+    assert _q4(L, ts=None) == fb.ERR_INVALID_ARG
+    assert _q4(L, ldq=32) == fb.ERR_INVALID_ARG  # ld_q < cols / 2
+    assert _q4(L, x=MIS) == fb.ERR_ALIGNMENT
+    assert _q4(L, ldx=132) == fb.ERR_ALIGNMENT
+    assert _q4(L, ldq=68) == fb.ERR_ALIGNMENT
+    assert _q4(L, ws=None) == fb.ERR_WORKSPACE  # two-pass needs the amax workspace
+    assert _q4(L, wsb=16) == fb.ERR_WORKSPACE
+    assert _q4(L, st=MIS, ws=None) == fb.ERR_ALIGNMENT  # static s_t: no workspace, aligned float
+    d = L.fp8_dequantize_nvfp4
+    assert d(A16, 0, 128, 64, 0, A16, A16, A16b, 128, None) == fb.OK
+    assert d(A16, 8, 128, 64, 3, A16, A16, A16b, 128, None) == fb.ERR_INVALID_ARG
+    assert d(A16, 8, 100, 64, 0, A16, A16, A16b, 128, None) == fb.ERR_UNSUPPORTED_SHAPE
+    assert d(A16, 8, 128, 64, 0, None, A16, A16b, 128, None) == fb.ERR_INVALID_ARG
+    assert d(A16, 8, 128, 64, 0, A16, A16, MIS, 128, None) == fb.ERR_ALIGNMENT
+    g = L.fp8_gemm_nvfp4
+    assert g(A16, A16, A16, A16b, A16, A16, A16, 0, 16, 256, None, None) == fb.OK
+    assert g(A16, A16, A16, A16b, A16, A16, A16, 16, 16, 128, None, None) == fb.ERR_UNSUPPORTED_SHAPE  # K % 256
+    assert g(A16, A16, A16, A16b, A16, A16, A16, 16, 24, 256, None, None) == fb.ERR_UNSUPPORTED_SHAPE  # N % 16
+    assert g(A16, None, A16, A16b, A16, A16, A16, 16, 16, 256, None, None) == fb.ERR_INVALID_ARG
+    assert g(A16, A16, None, A16b, A16, A16, A16, 16, 16, 256, None, None) == fb.ERR_INVALID_ARG
+    assert g(A16, MIS, A16, A16b, A16, A16, A16, 16, 16, 256, None, None) == fb.ERR_ALIGNMENT
+    assert g(A16, A16, A16, A16b, A16, A16, A16, 16, 16, 256, MIS, None) == fb.ERR_ALIGNMENT
+    p = L.fp8_debug_gemm_blockscaled_pairs
+    assert p(A16, A16, A16b, A16, 0, 0, A16, 16, 16, 144, None, None) == fb.ERR_UNSUPPORTED_SHAPE  # K % 128
+    assert p(A16, None, A16b, A16, 0, 0, A16, 16, 16, 128, None, None) == fb.ERR_INVALID_ARG
+    assert p(A16, MIS, A16b, A16, 0, 0, A16, 16, 16, 128, None, None) == fb.ERR_ALIGNMENT
+    assert p(A16, A16, A16b, A16, 0, 0, A16, 0, 16, 128, None, None) == fb.OK
+    e = L.fp8_debug_encode_e2m1_f32
+    assert e(A16, 12, A16b, None) == fb.ERR_INVALID_ARG
+    assert e(MIS, 16, A16b, None) == fb.ERR_ALIGNMENT
+    assert e(A16, 0, A16b, None) == fb.OK
+    assert fb.launch_count() == n0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(fb, "_lib", None)
     monkeypatch.setattr(fb, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libfp8bs.so"))
