@@ -101,13 +101,25 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
 #define FOLD_USE_PAIRS 0  // 1: block-scaled GEMMs with M > 128 run on CTA pairs (measured slower)
 #endif
 
+#ifndef FOLD_BF16_BN
+#define FOLD_BF16_BN 256  // bf16-output fold GEMM: 256 (two partial buffers) or 128 (four)
+#endif
+
+#ifndef FOLD_MMA_ISSUERS
+#define FOLD_MMA_ISSUERS 2  // threads (in warps 1..) issuing the fold kernels' MMAs, k-blocks dealt round robin
+#endif
+
+#ifndef FOLD_SCALE_AHEAD
+#define FOLD_SCALE_AHEAD 2  // k-blocks between a fold's scale loads and their use
+#endif
+
 #ifndef FOLD_CHUNK
 #define FOLD_CHUNK 64  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
 #endif
 
 // acc[base + i] += sc * (r[2i], r[2i+1]) for i < CH/2, as packed fp32x2 FMAs.
-template <int CH>
-__device__ __forceinline__ void fold_chunk(float2 (&acc)[64], int base, float2 sc2, const uint32_t (&r)[CH]) {
+template <int CH, int NA>
+__device__ __forceinline__ void fold_chunk(float2 (&acc)[NA], int base, float2 sc2, const uint32_t (&r)[CH]) {
 #pragma unroll
   for (int i = 0; i < CH / 2; ++i)
     acc[base + i] = __ffma2_rn(sc2, make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), acc[base + i]);
@@ -141,19 +153,33 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
 // =====================================================================
 // Fold kernel: 1x128 x 128x128 scales, per-chunk fp32 fold in registers
 // =====================================================================
-// Warp layout (12 warps): warpgroup 0 = producer (warp 0), MMA issuer and
-// tensor-memory owner (warp 1), two idle warps; warpgroups 1-2 = fold warps.
-// The fold warps keep 128 fp32 accumulators each and get most of the register
-// file (setmaxnreg), the other warpgroup gives registers back.
-template <int BN, int STAGES>
+// Warp layout: warpgroup 0 = producer (warp 0), tensor-memory owner and MMA
+// issuer (warp 1), second MMA issuer (warp 2), one idle warp; the other
+// warpgroups are fold warps. One thread issuing every k-block's four MMAs,
+// its commit and its two barrier waits needed ~800 cycles per k-block against
+// 512 of tensor work; two issuers taking alternate k-blocks (each owning one
+// partial buffer, so a buffer's MMAs stay in issue order) overlap that work. NBUF
+// partial buffers of BN columns sit in tensor memory (NBUF x BN <= 512): with
+// two, the fold of k-block kc gates the MMA of kc + 2; with four (128-wide
+// tiles) the MMA may run four k-blocks ahead of the fold. Each fold thread
+// owns WC columns of one row (128 with two buffers; 64 with four, so that
+// eight warps share the tensor-memory reads of a 128-wide tile). The fold
+// warps get most of the register file (setmaxnreg), the other warpgroup gives
+// registers back.
+template <int BN, int STAGES, int NBUF = 2>
 struct FoldCfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int CONSUMER_WARPS = 4 * (BN / 128);  // each thread folds 128 columns of one row
+  static constexpr int WC = NBUF == 4 ? 64 : 128;        // columns per fold thread
+  static constexpr int CONSUMER_WARPS = 4 * (BN / WC);  // 4 lane quarters x BN / WC column slabs
   static constexpr int FIRST_CONSUMER_WARP = 4;
   static constexpr int THREADS = 32 * (FIRST_CONSUMER_WARP + CONSUMER_WARPS);
-  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static_assert(NBUF * BN <= 512 && (NBUF == 2 || NBUF == 4), "partial buffers exceed tensor memory");
+  // the fold warps wait on the stage barrier by parity: k-block kc + STAGES
+  // cannot complete before they have released the buffer of kc + STAGES - NBUF
+  static_assert(STAGES >= NBUF, "stage barrier parity needs STAGES >= NBUF");
+  static constexpr uint32_t TMEM_COLS = NBUF * BN <= 256 ? 256 : 512;
   // output staging for the TMA-store epilogue: EPI_SLOTS 4 KB slots per fold
   // warp (two make the epilogue wait-free), as many as the shared memory left
   // by the stages holds
@@ -167,7 +193,7 @@ struct FoldCfg {
   // in that pool or the increase never completes; launch_fold_tiles checks it
   // against the compiled register count before launching.
   static constexpr uint32_t REGS_CONTROL = 40;
-  static constexpr uint32_t REGS_FOLD = BN == 256 ? 224 : 240;
+  static constexpr uint32_t REGS_FOLD = CONSUMER_WARPS == 8 ? 224 : 240;
   static constexpr uint32_t REGS_NEEDED = REGS_CONTROL * 32 * FIRST_CONSUMER_WARP + REGS_FOLD * 32 * CONSUMER_WARPS;
 };
 
@@ -190,10 +216,12 @@ bool reg_split_fits(KernelT kernel, int threads, uint32_t needed) {
 // mid() runs once the first store is issued, while that store reads shared
 // memory (the caller issues the next tile's first scale loads there, so their
 // latency hides behind the rest of the epilogue).
-template <int QFMT, int NSLOTS, typename Mid>
-__device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int row0, int n0, int M, int N,
+template <int QFMT, int NSLOTS, int NA, typename Mid>
+__device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[NA], int m, int row0, int n0, int M, int N,
                                                   const CUtensorMap *tmo, uint8_t *slots, float *q_scales,
                                                   int lane, Mid &&mid) {
+  static_assert(NA == 32 || NA == 64, "32 or 64 column pairs per thread");
+  static_assert(QFMT < 0 || NA == 64, "the quantized output needs a whole 1x128 group per thread");
   const bool rows_in = row0 < M;
   uint8_t *my_row = slots + lane * 128;
   const int swz = lane & 7;
@@ -201,11 +229,11 @@ __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int 
   if (lane == 0) bulk_wait_read_all();
   __syncwarp();
   if constexpr (QFMT < 0) {
-    uint32_t p[64];
+    uint32_t p[NA];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) p[i] = pack_bf16x2(acc[i].x, acc[i].y);
+    for (int i = 0; i < NA; ++i) p[i] = pack_bf16x2(acc[i].x, acc[i].y);
 #pragma unroll
-    for (int bx = 0; bx < 2; ++bx) {
+    for (int bx = 0; bx < NA / 32; ++bx) {
       uint8_t *row = my_row + (bx % NSLOTS) * 4096;
       if (bx >= NSLOTS) {
         if (lane == 0) bulk_wait_read_all();
@@ -261,21 +289,23 @@ __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[64], int m, int 
 // QFMT < 0: bf16 output. QFMT = FP8_E4M3 / FP8_E5M2: the epilogue quantizes
 // its own bf16-rounded output with 1x128 scales (the next layer's activation
 // format) and writes codes + scales instead of bf16.
-template <int BN, int STAGES, int QFMT>
-__global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
+template <int BN, int STAGES, int QFMT, int NBUF>
+__global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
     gemm_fold_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const float *__restrict__ sa,
                      const float *__restrict__ sb, float *__restrict__ q_scales, int M, int N, int K, uint32_t idesc,
                      int *dev_status, int group_m) {
-  using C = FoldCfg<BN, STAGES>;
+  using C = FoldCfg<BN, STAGES, NBUF>;
+  constexpr int ISSUERS = FOLD_MMA_ISSUERS;
+  static_assert(ISSUERS >= 1 && ISSUERS <= 3 && NBUF % ISSUERS == 0, "each partial buffer needs one issuer");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   // One commit per k-block: empty[s] completes when the MMAs of the k-block in
   // stage s are done, which frees the stage for the producer and tells the fold
   // warps that the partial of that k-block is in tensor memory. The fold warps
   // can wait on it by parity because the stage's next k-block (kc + STAGES)
-  // cannot complete before they release its buffer after k-block kc + 2.
-  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[2], drain;
+  // cannot complete before they release the buffer of k-block kc + STAGES - NBUF.
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[NBUF], drain;
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -291,8 +321,8 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&tempty[b], C::CONSUMER_WARPS);
-    mbar_init(&drain, 1);
+    for (int b = 0; b < NBUF; ++b) mbar_init(&tempty[b], C::CONSUMER_WARPS);
+    mbar_init(&drain, ISSUERS);
     ctl.abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -335,14 +365,19 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
         flag_abort(&ctl, dev_status);
         drain_stages<STAGES>(full, it);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp >= 1 && warp <= ISSUERS && lane == 0) {
+      // MMA issuers: issuer j takes the k-blocks with kc % ISSUERS == j, so each
+      // partial buffer is written by one thread only (its MMAs stay in order)
+      // while the issue work of consecutive k-blocks overlaps
+      const int me = warp - 1;
       int it = 0, kc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
-          const int b = kc & 1;
+          if (ISSUERS > 1 && kc % ISSUERS != me) continue;
+          const int b = kc % NBUF;
           const int s = it % STAGES;
-          if (!mbar_wait(&tempty[b], ((kc >> 1) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
+          if (!mbar_wait(&tempty[b], ((kc / NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
               !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
             ok = false;
             break;
@@ -365,63 +400,68 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
     regs_alloc<C::REGS_FOLD>();
     // ------------------------------------------------ fold consumers
     const int cw = warp - C::FIRST_CONSUMER_WARP;
+    constexpr int WC = C::WC;
     const int quarter = warp & 3;  // tensor-memory lanes this warp may access
-    const int half = cw >> 2;      // which 128-column half of the tile
+    const int half = cw >> 2;      // which WC-column slab of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     int kc = 0;
     bool ok = true;
-    float2 acc[64];
-    // first two scale pairs of a tile: loaded in the previous tile's epilogue
-    // (see fold_epilogue_tma), else at the top of the tile
-    auto first_scales = [&](int t, float &a0, float &b0, float &a1, float &b1) {
+    float2 acc[WC / 2];
+    // Scales are loaded SA k-blocks ahead of their fold (a register ring); the
+    // first SA pairs of a tile are loaded in the previous tile's epilogue (see
+    // fold_epilogue_tma), else at the top of the tile.
+    constexpr int SA = FOLD_SCALE_AHEAD;
+    auto first_scales = [&](int t, float (&a)[SA], float (&b)[SA]) {
       int tm, tn;
       tile_coords(t, num_m, num_n, group_m, tm, tn);
       const int tr = tm * BM + quarter * 32 + lane;
-      const int tb = tn * (BN / 128) + half;
+      const int tb = (tn * BN + half * WC) / 128;
       const float *pa = sa + tr;
       const float *pb = sb + static_cast<int64_t>(tb) * KB;
-      a0 = tr < M ? __ldg(pa) : 0.0f;
-      b0 = tb < nblk128 ? __ldg(pb) : 0.0f;
-      a1 = (tr < M && KB > 1) ? __ldg(pa + static_cast<int64_t>(M)) : 0.0f;
-      b1 = (tb < nblk128 && KB > 1) ? __ldg(pb + 1) : 0.0f;
+#pragma unroll
+      for (int j = 0; j < SA; ++j) {
+        a[j] = (tr < M && j < KB) ? __ldg(pa + static_cast<int64_t>(j) * M) : 0.0f;
+        b[j] = (tb < nblk128 && j < KB) ? __ldg(pb + j) : 0.0f;
+      }
     };
-    float nsa0 = 0.0f, nsb0 = 0.0f, nsa1 = 0.0f, nsb1 = 0.0f;
+    float nsa[SA], nsb[SA];
     bool have_next = false;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, num_m, num_n, group_m, mt, nt);
       const int m = mt * BM + quarter * 32 + lane;
       const bool row_ok = m < M;
-      const int nb = nt * (BN / 128) + half;
+      const int nb = (nt * BN + half * WC) / 128;  // weight block of this slab
       const bool col_ok = nb < nblk128;
       const float *sa_row = sa + m;
       const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      // scale prefetch, two chunks ahead
-      float sa0, sb0, sa1, sb1;
+      for (int i = 0; i < WC / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
+      // scales of k-blocks kb .. kb + SA - 1
+      float sa_ring[SA], sb_ring[SA];
       if (have_next) {
-        sa0 = nsa0;
-        sb0 = nsb0;
-        sa1 = nsa1;
-        sb1 = nsb1;
+#pragma unroll
+        for (int j = 0; j < SA; ++j) {
+          sa_ring[j] = nsa[j];
+          sb_ring[j] = nsb[j];
+        }
       } else {
-        first_scales(tile, sa0, sb0, sa1, sb1);
+        first_scales(tile, sa_ring, sb_ring);
       }
       for (int kb = 0; kb < KB; ++kb, ++kc) {
-        const int b = kc & 1;
-        const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
-        const float sb2 = (col_ok && kb + 2 < KB) ? __ldg(sb_blk + kb + 2) : 0.0f;
+        const int b = kc % NBUF;
+        const float sa_next = (row_ok && kb + SA < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + SA) * M) : 0.0f;
+        const float sb_next = (col_ok && kb + SA < KB) ? __ldg(sb_blk + kb + SA) : 0.0f;
         const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float sc = sa0 * sb0;
+        const float sc = sa_ring[0] * sb_ring[0];
         const float2 sc2 = make_float2(sc, sc);
-        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BN + half * 128);
-        constexpr int CH = FOLD_CHUNK, NCH = 128 / FOLD_CHUNK;
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BN + half * WC);
+        constexpr int CH = FOLD_CHUNK < WC ? FOLD_CHUNK : WC, NCH = WC / CH;
         if constexpr (CH >= 64) {
           // few large loads, one round trip each: load, wait, fold
 #pragma unroll
@@ -457,18 +497,21 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES>::THREADS, 1)
             }
           }
         }
-        sa0 = sa1;
-        sb0 = sb1;
-        sa1 = sa2;
-        sb1 = sb2;
+#pragma unroll
+        for (int j = 0; j + 1 < SA; ++j) {
+          sa_ring[j] = sa_ring[j + 1];
+          sb_ring[j] = sb_ring[j + 1];
+        }
+        sa_ring[SA - 1] = sa_next;
+        sb_ring[SA - 1] = sb_next;
       }
       if (!ok) break;
       const int next = tile + static_cast<int>(gridDim.x);
-      fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * BM + quarter * 32, nb * 128, M, N, &tmO,
+      fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * BM + quarter * 32, nt * BN + half * WC, M, N, &tmO,
                                             smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
                                             lane, [&]() {
                                               have_next = next < ntiles;
-                                              if (have_next) first_scales(next, nsa0, nsb0, nsa1, nsb1);
+                                              if (have_next) first_scales(next, nsa, nsb);
                                             });
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
@@ -524,6 +567,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
                           const float *__restrict__ sb, float *__restrict__ q_scales, int M, int N, int K,
                           uint32_t idesc, int *dev_status, int group_m) {
   using C = FoldPairCfg<STAGES>;
+  constexpr int ISSUERS = FOLD_MMA_ISSUERS;
+  static_assert(ISSUERS == 1 || ISSUERS == 2, "each partial buffer needs one issuer");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   // one commit per k-block (multicast to both CTAs' empty[s]), as in the
@@ -549,7 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) mbar_init(&tempty[b], 2 * C::CONSUMER_WARPS);  // both CTAs' fold warps release to the even CTA
-    mbar_init(&drain, 1);
+    mbar_init(&drain, ISSUERS);
     ctl.abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -600,11 +645,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
           }
         }
       }
-    } else if (warp == 1 && lane == 0 && leader) {
+    } else if (warp >= 1 && warp <= ISSUERS && lane == 0 && leader) {
+      // pair MMA issuers, k-blocks dealt round robin as in the single-CTA kernel
+      const int me = warp - 1;
       int it = 0, kc = 0;
       bool ok = true;
       for (int tile = pair; tile < ntiles && ok; tile += npairs) {
         for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+          if (ISSUERS > 1 && kc % ISSUERS != me) continue;
           const int b = kc & 1;
           const int s = it % STAGES;
           if (!mbar_wait(&tempty[b], ((kc >> 1) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
@@ -1653,44 +1701,45 @@ bool use_pairs(int64_t M, int64_t N) {
   return FOLD_USE_PAIRS && M > 128 && 2 * pair_tiles >= device_sm_count();
 }
 
+template <int BN, int ST, int NBUF, int QFMT>
+fp8_status_t launch_fold_cfg(const CUtensorMap &ta, const CUtensorMap &to, const uint8_t *b, const float *sa,
+                             const float *sb, float *q_scales, int a_fmt, int b_fmt, int64_t M, int64_t N, int64_t K,
+                             int *dev_status, cudaStream_t stream) {
+  using C = FoldCfg<BN, ST, NBUF>;
+  CUtensorMap tb;
+  if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
+  auto kern = gemm_fold_kernel<BN, ST, QFMT, NBUF>;
+  if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
+  const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
+  if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, ta, tb, to,
+                       sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                       idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K)) != cudaSuccess)
+    return FP8_ERR_CUDA;
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 template <int QFMT>
 fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                                int b_fmt, uint16_t *out, uint8_t *q_out, float *q_scales, int64_t M, int64_t N,
                                int64_t K, int *dev_status, cudaStream_t stream) {
-  // Wide tiles when there are enough of them to fill the GPU, else 128-wide.
-  const int sms = device_sm_count();
-  const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
-  const bool wide = tiles256 >= sms;
-  CUtensorMap ta, tb, to;
+  CUtensorMap ta, to;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK)) return FP8_ERR_CUDA;
   // output boxes: 32 rows x 128 bytes (bf16: 64 columns; fp8 codes: 128)
   if (QFMT < 0 ? !make_tmap_u16(&to, out, M, N, N, 32, 64) : !make_tmap_u8(&to, q_out, M, N, N, 32, 128))
     return FP8_ERR_CUDA;
-  if (wide) {
-    constexpr int BN = 256, ST = FOLD_WIDE_STAGES;
-    using C = FoldCfg<BN, ST>;
-    if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-    auto kern = gemm_fold_kernel<BN, ST, QFMT>;
-    if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
-    const int ntiles = static_cast<int>(tiles256);
-    if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, ta, tb,
-                         to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K)) != cudaSuccess)
-      return FP8_ERR_CUDA;
+  if constexpr (QFMT < 0 && FOLD_BF16_BN == 128) {
+    // 128-wide tiles, four partial buffers: the MMA runs up to four k-blocks
+    // ahead of the fold
+    return launch_fold_cfg<128, 6, 4, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K, dev_status, stream);
   } else {
-    constexpr int BN = 128, ST = 6;
-    using C = FoldCfg<BN, ST>;
-    if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-    auto kern = gemm_fold_kernel<BN, ST, QFMT>;
-    if (!ensure_smem(kern, C::SMEM) || !reg_split_fits(kern, C::THREADS, C::REGS_NEEDED)) return FP8_ERR_CUDA;
-    const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + 127) / 128));
-    if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, ta, tb,
-                         to, sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                         idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K)) != cudaSuccess)
-      return FP8_ERR_CUDA;
+    // Wide tiles when there are enough of them to fill the GPU, else 128-wide.
+    const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+    if (tiles256 >= device_sm_count())
+      return launch_fold_cfg<256, FOLD_WIDE_STAGES, 2, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K,
+                                                             dev_status, stream);
+    return launch_fold_cfg<128, 6, 2, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K, dev_status, stream);
   }
-  note_launches(1);
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 }  // namespace
