@@ -832,6 +832,10 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // dependent launch: the setup above overlaps the previous kernel's tail;
+  // nothing it writes (X, the scales, Out) is touched before this wait
+  grid_dependents_launch();
+  grid_dependency_wait();
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
@@ -1040,6 +1044,8 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
   __syncthreads();
   cluster_sync();  // every CTA's barriers exist before any remote arrive
   tc_fence_after();
+  grid_dependents_launch();  // as in the unsplit kernel
+  grid_dependency_wait();
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
@@ -1581,6 +1587,25 @@ int persistent_grid(int ntiles) {
   return ntiles < sms ? ntiles : sms;
 }
 
+// Launch with programmatic stream serialization: the kernel may begin (and do
+// its setup) while the previous kernel in the stream finishes; it waits for
+// that kernel's results with grid_dependency_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // K splits for the decode kernel. Without a split, a tile is one 128-row W block
 // streamed over all of K by one CTA, and when there are fewer tiles than SMs the
 // idle SMs' share of HBM bandwidth is lost. With S splits the tile's K range is
@@ -1629,13 +1654,15 @@ fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *
       cfg.blockDim = dim3(CS::THREADS, 1, 1);
       cfg.dynamicSmemBytes = CS::SMEM;
       cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
+      cudaLaunchAttribute attr[2];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = static_cast<unsigned>(S);
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      cfg.numAttrs = 2;
       const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tx, tw, sa, sb, out, static_cast<int>(M),
                                                static_cast<int>(N), static_cast<int>(K), idesc, dev_status);
       note_launches(1);
@@ -1645,9 +1672,10 @@ fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *
   using C = SwapCfg<BX, ST>;
   auto kern = gemm_fold_swap_kernel<BX, ST>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
-  kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(tx, tw, sa, sb, out, static_cast<int>(M),
-                                                                 static_cast<int>(N), static_cast<int>(K), idesc,
-                                                                 dev_status);
+  if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, tx, tw,
+                       sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), idesc,
+                       dev_status) != cudaSuccess)
+    return FP8_ERR_CUDA;
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -1674,25 +1702,6 @@ fp8_status_t launch_fold_pairs(const uint8_t *a, const float *sa, const uint8_t 
       idesc_f8f6f4(a_fmt, b_fmt, 256, 256), dev_status, static_cast<int>(g));
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
-}
-
-// Launch with programmatic stream serialization: the kernel may begin (and do
-// its setup) while the previous kernel in the stream finishes; it waits for
-// that kernel's results with grid_dependency_wait().
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
-                             Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(block, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // CTA pairs need at least 256 rows and enough pair tiles to fill the GPU.
