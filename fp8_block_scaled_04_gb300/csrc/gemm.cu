@@ -377,18 +377,22 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
           if (ISSUERS > 1 && kc % ISSUERS != me) continue;
           const int b = kc % NBUF;
           const int s = it % STAGES;
-          if (!mbar_wait(&tempty[b], ((kc / NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
-              !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint64_t adesc = sdesc_k_sw128(a0), bdesc = sdesc_k_sw128(a0 + C::A_BYTES);
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+          // the stage's operands first (they usually landed long before), then
+          // the partial buffer: the fold's release is the critical path, and a
+          // wait on an already completed barrier still costs ~100 cycles
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort) ||
+              !mbar_wait(&tempty[b], ((kc / NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t b0 = a0 + C::A_BYTES;
-          const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+          // K step k: both descriptors advance 32 bytes (2 units of 16 bytes)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            mma_f8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
           tc_commit(&empty[s]);
         }
       }
