@@ -1424,6 +1424,11 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
         const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE_STRIDE);
+          const uint32_t b0 = a0 + C::A_BYTES;
+          // descriptors formed before the waits (the MMAs follow the last wait
+          // directly); K step k advances both by 32 bytes (2 units of 16)
+          const uint64_t adesc = sdesc_k_sw128(a0), bdesc = sdesc_k_sw128(b0);
           // the operands, and (block-scaled kinds) the scale atoms in tensor
           // memory; without SF_SPLIT sf_ready[s] implies full[s]
           if ((!C::COPIER || C::SF_SPLIT) && !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
@@ -1435,8 +1440,6 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + s * C::STAGE_STRIDE);
-          const uint32_t b0 = a0 + C::A_BYTES;
           if constexpr (MX && !C::COPIER)
             copy_scale_atoms<KIND, BN>(tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS), b0 + C::B_BYTES);
           if (F4) {
@@ -1447,20 +1450,20 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
             const uint32_t sfb_t = sfa_t + 16;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_mxf4nvf4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, sfa_t + 4 * k,
+              mma_mxf4nvf4(d, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_t + 4 * k,
                            sfb_t + 8 * k, (kb > 0 || k > 0) ? 1u : 0u);
           } else if (MX) {
             const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
             const uint32_t sfb_t = sfa_t + 4;
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k)
-              mma_mxf8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k),
+              mma_mxf8f6f4(d, adesc + 2 * k, bdesc + 2 * k,
                            idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29), sfa_t, sfb_t,
                            (kb > 0 || k > 0) ? 1u : 0u);
           } else {
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k)
-              mma_f8f6f4(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc,
+              mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc,
                          (kb > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);
