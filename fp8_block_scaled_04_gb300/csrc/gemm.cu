@@ -1254,32 +1254,31 @@ struct AccCfg {
   static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory budget");
 };
 
-// A stage's scale atoms, shared memory (sf_smem: A's atoms, then B's per
-// 128-row block) -> tensor memory (sf_tmem). MXFP8: one atom per 128 rows at
-// +4 columns per block. NVFP4: four atoms per 128 rows; A's atom k at +4k, B's
-// at +8k (+4 for the second 128-row block).
+// A stage's scale atoms, shared memory (A's atoms, then B's per 128-row block;
+// sf_desc: descriptor of the first atom, an atom 512 bytes further on is 32
+// units of 16 bytes further) -> tensor memory (sf_tmem). MXFP8: one atom per
+// 128 rows at +4 columns per block. NVFP4: four atoms per 128 rows; A's atom k
+// at +4k, B's at +8k (+4 for the second 128-row block).
 // With several copiers, copier `part` of `nparts` issues the atoms whose index
 // (in the order below) is congruent to part.
 template <int KIND, int BN>
-__device__ __forceinline__ void copy_scale_atoms(uint32_t sf_tmem, uint32_t sf_smem, int part = 0, int nparts = 1) {
+__device__ __forceinline__ void copy_scale_atoms(uint32_t sf_tmem, uint64_t sf_desc, int part = 0, int nparts = 1) {
+  constexpr uint64_t ATOM = 512 >> 4;
   if constexpr (KIND == KIND_NVF4) {
     constexpr int PER_K = 1 + BN / 128;  // A's atom, then B's per 128-row block
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      if ((k * PER_K) % nparts == part)
-        tmem_cp_32x128b_warpx4(sf_tmem + 4 * k, sdesc_plain_32x16(sf_smem + 512 * k));
+      if ((k * PER_K) % nparts == part) tmem_cp_32x128b_warpx4(sf_tmem + 4 * k, sf_desc + ATOM * k);
 #pragma unroll
       for (int j = 0; j < BN / 128; ++j)
         if ((k * PER_K + 1 + j) % nparts == part)
-          tmem_cp_32x128b_warpx4(sf_tmem + 16 + 8 * k + 4 * j,
-                                 sdesc_plain_32x16(sf_smem + 2048 + 2048 * j + 512 * k));
+          tmem_cp_32x128b_warpx4(sf_tmem + 16 + 8 * k + 4 * j, sf_desc + ATOM * (4 + 4 * j + k));
     }
   } else {
-    if (part == 0) tmem_cp_32x128b_warpx4(sf_tmem, sdesc_plain_32x16(sf_smem));
+    if (part == 0) tmem_cp_32x128b_warpx4(sf_tmem, sf_desc);
 #pragma unroll
     for (int j = 0; j < BN / 128; ++j)
-      if ((1 + j) % nparts == part)
-        tmem_cp_32x128b_warpx4(sf_tmem + 4 + 4 * j, sdesc_plain_32x16(sf_smem + 512 + 512 * j));
+      if ((1 + j) % nparts == part) tmem_cp_32x128b_warpx4(sf_tmem + 4 + 4 * j, sf_desc + ATOM * (1 + j));
   }
 }
 
@@ -1394,13 +1393,13 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
+          const uint64_t sf_desc = sdesc_plain_32x16(smem_u32(smem + s * C::STAGE_STRIDE) + C::A_BYTES + C::B_BYTES);
           if (!mbar_wait(C::SF_SPLIT ? &sf_full[s] : &full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          copy_scale_atoms<KIND, BN>(tmem + static_cast<uint32_t>(C::ACC_COLS + s * C::SF_COLS),
-                                     smem_u32(smem + s * C::STAGE_STRIDE) + C::A_BYTES + C::B_BYTES, part,
+          copy_scale_atoms<KIND, BN>(tmem + static_cast<uint32_t>(C::ACC_COLS + s * C::SF_COLS), sf_desc, part,
                                      C::COPIERS);
           tc_commit(&sf_ready[s]);
         }
@@ -1441,7 +1440,8 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
           }
           tc_fence_after();
           if constexpr (MX && !C::COPIER)
-            copy_scale_atoms<KIND, BN>(tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS), b0 + C::B_BYTES);
+            copy_scale_atoms<KIND, BN>(tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS),
+                                       sdesc_plain_32x16(b0 + C::B_BYTES));
           if (F4) {
             // NVFP4: one scale atom per MMA (K = 64, four 16-element scales per
             // row); A's atom k at column +4k, B's at +8k (second 128-row block
