@@ -873,18 +873,19 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
           const int b = kc % C::NBUF;
           const int s = it % STAGES;
+          const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint64_t wdesc = sdesc_k_sw128(w0), xdesc = sdesc_k_sw128(w0 + C::W_BYTES);
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
+          // the partial buffer (usually free) before the stage (the copy in
+          // flight from HBM is the critical wait); descriptors formed first
           if (!mbar_wait(&tempty[b], ((kc / C::NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
               !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t x0 = w0 + C::W_BYTES;
-          const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_f8f6f4(d, sdesc_k_sw128(w0 + 32 * k), sdesc_k_sw128(x0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+          for (int k = 0; k < BK / 32; ++k) mma_f8f6f4(d, wdesc + 2 * k, xdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
           tc_commit(&empty[s]);
         }
       }
@@ -1083,18 +1084,19 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++it, ++kc) {
           const int b = kc % C::NBUF;
           const int s = it % STAGES;
+          const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint64_t wdesc = sdesc_k_sw128(w0), xdesc = sdesc_k_sw128(w0 + C::W_BYTES);
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
+          // the partial buffer (usually free) before the stage (the copy in
+          // flight from HBM is the critical wait); descriptors formed first
           if (!mbar_wait(&tempty[b], ((kc / C::NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
               !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t x0 = w0 + C::W_BYTES;
-          const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_f8f6f4(d, sdesc_k_sw128(w0 + 32 * k), sdesc_k_sw128(x0 + 32 * k), idesc, k > 0 ? 1u : 0u);
+          for (int k = 0; k < BK / 32; ++k) mma_f8f6f4(d, wdesc + 2 * k, xdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
           tc_commit(&empty[s]);
         }
       }
