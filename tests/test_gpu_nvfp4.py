@@ -62,6 +62,34 @@ def test_quantize_static_scale_and_extremes():
         assert np.array_equal(sf, sfo), static
 
 
+def _e4m3_midpoint_blocks():
+    """bf16 rows of 16-element blocks whose amax is 3 (v_i + v_i+1) for consecutive
+    E4M3 values v_i < v_i+1 (exact in bf16): with s_t = 1 the block scale
+    amax / 6 / s_t is exactly their midpoint, a rounding tie."""
+    vals = sorted({float(v) for v in oracle.decode(np.arange(0x00, 0x7f, dtype=np.uint8), oracle.E4M3)})
+    amax = np.array([3.0 * (a + b) for a, b in zip(vals[:-1], vals[1:])], dtype=np.float32)
+    x = np.zeros((len(amax), 16), dtype=np.float32)
+    x[:, 5] = amax
+    x[:, 9] = -0.5 * amax
+    bits = oracle.f32_to_bf16(x)
+    assert np.array_equal(oracle.bf16_to_f32(bits), x)  # exactly representable
+    return bits.reshape(-1, 64) if len(amax) % 4 == 0 else bits[: len(amax) // 4 * 4].reshape(-1, 64)
+
+
+@pytest.mark.parametrize("k", list(range(-12, 13)))
+def test_quantize_block_scales_near_e4m3_midpoints(k):
+    """Static tensor scales 1 +- k units in the last place move every block scale a
+    few fp32 units off an E4M3 rounding midpoint: the band where the encoder's
+    multiply-by-reciprocal step must hand over to the exact divisions."""
+    x = _e4m3_midpoint_blocks()
+    s_t = float(np.float32(1.0 + k * 2.0 ** -23) if k >= 0 else np.float32(1.0 + k * 2.0 ** -24))
+    q, sf, ts = _quant_dev(x, fb.SF_LINEAR, s_t)
+    qo, sfo, tso = oracle.quantize_nvfp4(x, fb.SF_LINEAR, s_t)
+    assert np.float32(ts) == np.float32(tso)
+    assert np.array_equal(sf, sfo), k
+    assert np.array_equal(q, qo), k
+
+
 @pytest.mark.parametrize("layout", [fb.SF_LINEAR, fb.SF_TCGEN05])
 def test_dequantize_bit_exact(layout):
     rows, cols = 130, 1024
