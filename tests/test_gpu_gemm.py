@@ -11,7 +11,7 @@ import torch
 import oracle
 from fp8_block_scaled_04_gb300 import binding as fb
 from fp8_block_scaled_04_gb300 import synth
-from gpu_util import out_f64, to_dev_bf16, within_tolerance
+from gpu_util import bf16_host, out_f64, to_dev_bf16, within_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -213,3 +213,37 @@ def test_status_stays_zero_and_launches_counted():
     n0 = fb.launch_count()
     _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
     assert fb.launch_count() == n0 + 1
+
+
+@pytest.mark.parametrize("M", [16, 64, 256])
+def test_dependent_launches_keep_stream_order(M):
+    """quantize -> GEMM -> quantize -> GEMM -> GEMM enqueued with no host sync between
+    them. The GEMMs are dependent launches that may start before the kernel ahead of
+    them has finished; each stage, checked against the oracle on the GPU's own inputs
+    to it, must have read its producer's finished output."""
+    K1, N1, N2 = 1024, 2048, 1024
+    x = synth.bf16_matrix(M, K1, 1.0, 700 + M, 701, 0.01, 30.0)
+    w1 = synth.bf16_matrix(N1, K1, 0.02, 702)
+    w2 = synth.bf16_matrix(N2, N1, 0.02, 703)
+    w3 = synth.bf16_matrix(N2, N1, 0.02, 704)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    qw = [oracle.quantize(w, fb.E4M3, fb.BLOCK_128x128, fb.SF_LINEAR) for w in (w1, w2, w3)]
+    qw_d = [(dev(q), dev(sc)) for q, sc in qw]
+    torch.cuda.synchronize()
+    xq, xs = fb.quantize(to_dev_bf16(x), fb.E4M3, fb.TILE_1x128)
+    o1 = fb.gemm_blockscaled(xq, xs, fb.TILE_1x128, *qw_d[0], fb.BLOCK_128x128)
+    hq, hs = fb.quantize(o1, fb.E4M3, fb.TILE_1x128)
+    o2 = fb.gemm_blockscaled(hq, hs, fb.TILE_1x128, *qw_d[1], fb.BLOCK_128x128)
+    o3 = fb.gemm_blockscaled(hq, hs, fb.TILE_1x128, *qw_d[2], fb.BLOCK_128x128)
+    torch.cuda.synchronize()
+    xq_o, xs_o = oracle.quantize(x, fb.E4M3, fb.TILE_1x128, fb.SF_LINEAR)
+    assert np.array_equal(xq.cpu().numpy(), xq_o) and np.array_equal(xs.cpu().numpy(), xs_o)
+    ref, bound = oracle.gemm(xq_o, xs_o, fb.TILE_1x128, *qw[0], fb.BLOCK_128x128)
+    bad, worst = within_tolerance(out_f64(o1), ref, bound)
+    assert bad == 0, ("o1", bad, worst)
+    hq_o, hs_o = oracle.quantize(bf16_host(o1), fb.E4M3, fb.TILE_1x128, fb.SF_LINEAR)
+    assert np.array_equal(hq.cpu().numpy(), hq_o) and np.array_equal(hs.cpu().numpy(), hs_o)
+    for o, (qb, sb) in ((o2, qw[1]), (o3, qw[2])):
+        ref, bound = oracle.gemm(hq_o, hs_o, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+        bad, worst = within_tolerance(out_f64(o), ref, bound)
+        assert bad == 0, (bad, worst)
