@@ -28,6 +28,11 @@
  *     returns; the caller zeroes *dev_status beforehand and reads it after the
  *     stream completes. The library writes *dev_status only on error.
  *   - An empty problem (a zero dimension) is valid and enqueues nothing.
+ *   - Stream order holds as for ordinary launches. The block-scaled GEMM
+ *     kernels are launched as programmatic dependent launches: they may be
+ *     scheduled while the kernel ahead of them in the stream is finishing and
+ *     do their setup then, but they read no input (operands or scales) and
+ *     write no output before that kernel has completed.
  */
 #ifndef FP8BS_H
 #define FP8BS_H
