@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -45,16 +46,26 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
 
 
+def code_digest(text: str) -> str:
+    """sha256 of a C++/CUDA source with its comments, indentation and blank lines removed:
+    it changes whenever the code does, and not when only a comment does."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.strip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's source file has
+    the same code (comments aside) as when the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[kernel]
         src = os.path.join(ROOT, "fp8_block_scaled_04_gb300", "csrc", rec["source"])
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-        return float(rec["bytes_per_launch"]) if digest == rec["source_sha256"] else None
+        with open(src) as f:
+            digest = code_digest(f.read())
+        return float(rec["bytes_per_launch"]) if digest == rec["code_sha256"] else None
     except Exception:
         return None
 
