@@ -2,11 +2,13 @@
 //
 // Out[M x N] (bf16) = X[M x K] W[N x K]^T with FP8 operands and fp32
 // accumulation ("07 -- The FP8 Family", Scaling is what makes FP8 usable).
-// Three kernels share one warp-specialised, persistent structure:
-//   warp 0      TMA producer: operand tiles (and MX scale-factor atoms) into a
+// The kernels share one warp-specialised, persistent structure:
+//   warp 0      TMA producer: operand tiles (and scale-factor atoms) into a
 //               ring of shared-memory stages;
-//   warp 1      tensor-memory owner and MMA issuer (one elected thread);
-//   warps 2..   consumers that read tensor memory with tcgen05.ld.
+//   warp 1      tensor-memory owner and MMA issuer (one elected thread; the
+//               fold kernels add a second issuer in warp 2, alternate k-blocks);
+//   other warps scale-factor copiers (block-scaled kinds) and consumers that
+//               read tensor memory with tcgen05.ld.
 //
 // gemm_fold_kernel -- 1x128 activation tiles x 128x128 weight blocks (the
 //   DeepSeek-V3 scheme of "07 -- The FP8 Family"; the promotion paragraph of
@@ -14,6 +16,9 @@
 //   MMA group into a fresh tensor-memory buffer; the consumer warps fold it
 //   into fp32 registers as acc += (s_x[m,kb] * s_w[n/128,kb]) * partial. Two
 //   tensor-memory buffers let the MMA of chunk kb+1 run while chunk kb folds.
+//   gemm_fold_pair_kernel is the same on CTA pairs (cta_group::2); the
+//   gemm_fold_swap kernels take few activation rows (decode), with W on the
+//   MMA's 128-row side, optionally splitting K over a CTA cluster.
 // gemm_tmem_kernel<KIND_EPI> -- per-tensor / per-token / per-channel scales:
 //   the whole K sum stays in tensor memory and the scale product is applied
 //   once in the epilogue.
@@ -475,7 +480,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
             tmem_ld_chunk<CH>(taddr + CH * c, rb);
             tmem_wait_ld_regs(rb);
             if (c + 1 == NCH) {
-              // every load of this buffer has landed: hand it back to the MMA warp
+              // every load of this buffer has landed: hand it back to its MMA issuer
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&tempty[b]);
