@@ -62,8 +62,8 @@ def test_decode_gemm_full_size(decode_w, m):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
-    bad, worst = within_tolerance(out_f64(out), ref, bound)
-    assert bad == 0, (bad, worst)
+    tol = within_tolerance(out_f64(out), ref, bound)
+    assert tol.bad == 0, tol
 
 
 def test_prefill_gemm_full_size_sampled_rows():
@@ -82,8 +82,8 @@ def test_prefill_gemm_full_size_sampled_rows():
     rows = _sample_rows(M)
     ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, rows=rows)
     got = out_f64(out[torch.from_numpy(rows).cuda()])
-    bad, worst = within_tolerance(got, ref, bound)
-    assert bad == 0, (bad, worst)
+    tol = within_tolerance(got, ref, bound)
+    assert tol.bad == 0, tol
 
 
 def test_mx_gemm_full_size_sampled_rows():
@@ -102,5 +102,5 @@ def test_mx_gemm_full_size_sampled_rows():
     rows = _sample_rows(S, per_tile=1)
     ref, bound = oracle.gemm(qa, sfa, fb.MX32, qb, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05, rows=rows)
     got = out_f64(out[torch.from_numpy(rows).cuda()])
-    bad, worst = within_tolerance(got, ref, bound)
-    assert bad == 0, (bad, worst)
+    tol = within_tolerance(got, ref, bound)
+    assert tol.bad == 0, tol

@@ -355,3 +355,70 @@ def test_delayed_nonfinite_history_uses_unit_scale():
         assert s[0] == 1.0
         qs, _ = oracle.quantize(x, E4M3, TENSOR, static_scale=1.0)
         assert np.array_equal(q, qs)
+
+
+# ---------------------------------------------------------------- reading R2: x * fp32(1/s), not x / s
+# The pages print the quantize step both as x / s ("07 -- The FP8 Family", Scaling
+# is what makes FP8 usable; "FP8 Mixed-Precision Serving", per-tensor scaling
+# formula) and as a multiply by the reciprocal ("Low precision: FP8, FP4, and
+# microscaling", qdq_e4m3 listing). The two differ in fp32 for some (x, s): the
+# product and the quotient can land on opposite sides of an FP8 rounding
+# midpoint. The library takes the multiply. These witnesses are found from plain
+# fp32 arithmetic (numpy) and encoded with torch's float8 cast (round to nearest
+# even), so a divide anywhere in the oracle's encode step fails them.
+_R2_AMAX = (6528.0, 816.0, 210.0, 3120.0, 4016.0, 1.3046875, 0.76171875, 334.0, 3760.0, 97.5)
+
+
+def _r2_witnesses(fmt, amax, limit=6):
+    """bf16 x < amax whose multiply and divide forms encode differently, with the multiply's code."""
+    vmax = np.float32(VMAX[fmt])
+    s = np.float32(np.float32(amax) / vmax)
+    s_inv = np.float32(np.float32(1.0) / s)
+    bits = (np.arange(1, 0x7F80, dtype=np.uint32) << 16).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[x < np.float32(amax)]
+    dt = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}[fmt]
+
+    def cast(v):
+        return torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(dt).view(torch.uint8).numpy()
+
+    by_mul = cast((x * s_inv).astype(np.float32))
+    by_div = cast((x / s).astype(np.float32))
+    idx = np.nonzero(by_mul != by_div)[0][:limit]
+    return x[idx], by_mul[idx], by_div[idx]
+
+
+def test_r2_literal_witness_e4m3():
+    # amax 816: s = fp32(816/448) = 1.8214285373687744, fp32(1/s) = 0.5490196347236633.
+    # x = 0.037353515625 (bf16) times 1/s lies within an fp32 ulp of 0.0205078125, the
+    # midpoint between E4M3 0x0a (0.01953125) and 0x0b (0.021484375): the fp32
+    # product rounds above it (code 0x0b), the fp32 quotient x / s lands exactly on
+    # it and ties to the even code 0x0a.
+    s = np.float32(np.float32(816.0) / np.float32(448.0))
+    s_inv = np.float32(np.float32(1.0) / s)
+    x = np.float32(0.037353515625)
+    assert np.float32(x * s_inv) > np.float32(0.0205078125) == np.float32(x / s)
+    row = np.zeros((1, 128), dtype=np.float32)
+    row[0, 0], row[0, 5] = 816.0, x
+    q, sc = oracle.quantize(_bf16(row), E4M3, TOKEN)
+    assert sc[0] == s
+    assert q[0, 5] == 0x0B and q[0, 0] == 0x7E
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("gran", [TOKEN, TILE_1x128, TENSOR])
+def test_r2_multiply_by_reciprocal_not_divide(fmt, gran):
+    n_wit = 0
+    for amax in _R2_AMAX:
+        xs, mul, div = _r2_witnesses(fmt, amax)
+        if xs.size == 0:
+            continue
+        n_wit += xs.size
+        # one group (row / 1x128 tile / whole tensor) holding amax and the witnesses
+        row = np.zeros((1, 128), dtype=np.float32)
+        row[0, 0] = amax
+        row[0, 3:3 + xs.size] = xs
+        q, _ = oracle.quantize(_bf16(row), fmt, gran)
+        assert np.array_equal(q[0, 3:3 + xs.size], mul), (amax, xs, mul, div)
+        assert np.all(q[0, 3:3 + xs.size] != div)
+    assert n_wit >= 10
