@@ -90,12 +90,15 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
 // Per-tensor constants of the block-scale step. The block scale is
 // u = fp32(fp32(amax_b / 6) / s_t), and only its E4M3 rounding is kept. The
 // fast path forms u' = fp32(amax_b * c) with c = fp32(fp32(1/6) / s_t): each
-// of the five roundings involved is within 2^-24 relative, so |u' - u| is at
-// most 5 units in the last place of u, and when the 20 fp32 mantissa bits that
-// E4M3 discards are at least 6 units away from the rounding midpoint (and u'
-// is in E4M3's normal range below saturation) u and u' round to the same code.
-// Other blocks (about 1 in 10^5 in the midpoint band, plus zero, tiny and
-// non-finite ones) take the two IEEE divisions. s_inv of a code depends on
+// of the five roundings involved is within 2^-24 relative as long as every
+// intermediate is an fp32 normal -- c (checked per tensor), amax_b / 6 (so
+// amax_b >= 6 * 2^-126, checked per block: below it fp32(amax_b / 6) is
+// subnormal and its rounding error is far larger) and u' (>= 2^-6) -- so
+// |u' - u| is at most 5 units in the last place of u, and when the 20 fp32
+// mantissa bits that E4M3 discards are at least 6 units away from the rounding
+// midpoint (and u' is in E4M3's normal range below saturation) u and u' round
+// to the same code. Other blocks (about 1 in 10^5 in the midpoint band, plus
+// zero, tiny and non-finite ones) take the two IEEE divisions. s_inv of a code depends on
 // the code alone, so a table of the 256 codes replaces the per-block
 // reciprocal.
 struct BlockScaleStep {
@@ -131,7 +134,7 @@ __device__ __forceinline__ void encode_block(const uint4 v0, const uint4 v1, con
   const float amax_b = bf16_bits_to_f32(m);
   float u = __fmul_rn(amax_b, bs.c);
   const int d = static_cast<int>(__float_as_uint(u) & 0xfffffu) - 0x80000;
-  if (!(bs.fast && u >= 0.015625f && u <= 440.0f && (d >= 6 || d <= -6)))
+  if (!(bs.fast && amax_b >= 0x1.8p-124f && u >= 0.015625f && u <= 440.0f && (d >= 6 || d <= -6)))
     u = __fdiv_rn(__fdiv_rn(amax_b, 6.0f), bs.s_t);
   code = e4m3_code(u);
   const float s_inv = bs.s_inv[code];

@@ -62,6 +62,31 @@ def test_quantize_static_scale_and_extremes():
         assert np.array_equal(sf, sfo), static
 
 
+def test_quantize_tiny_static_tensor_scales_subnormal_blocks():
+    """Static tensor scales down to fp32 subnormals with bf16 block maxima around
+    6 * 2^-126, where fp32(amax_b / 6) is subnormal: bit-exact against the oracle's
+    two divisions. Rows 0-1 hold the blocks whose fast-step code would differ
+    (maxima 5 and 20 units of 2^-133 under s_t = fp32 bits 0x000A28A2)."""
+    rows, cols = 128, 256
+    bits = synth.bf16_matrix(rows, cols, 1.0, 931)
+    rng = np.random.default_rng(932)
+    small = np.arange(1, 0x0580, dtype=np.uint16)  # bf16 magnitudes up to ~64 * 2^-126, subnormals included
+    x = rng.choice(small, size=(rows, cols)).astype(np.uint16) | (rng.integers(0, 2, (rows, cols)) << 15).astype(np.uint16)
+    x[0, :16] = 0
+    x[0, 3] = 5
+    x[1, :16] = 0
+    x[1, 7] = 20
+    x[64:, :] = bits[64:, :] & 0x807F  # tiny normals / subnormals of mixed signs
+    s_wit = float(np.array([0x000A28A2], dtype=np.uint32).view(np.float32)[0])
+    for static in [s_wit, 5e-40, 1.335e-38, 2.0e-38, 4.7e-37]:
+        for layout in (fb.SF_LINEAR, fb.SF_TCGEN05):
+            q, sf, ts = _quant_dev(x, layout, static)
+            qo, sfo, tso = oracle.quantize_nvfp4(x, layout, static)
+            assert np.float32(ts) == np.float32(tso)
+            assert np.array_equal(sf[: sfo.size], sfo), (static, layout)
+            assert np.array_equal(q, qo), (static, layout)
+
+
 def _e4m3_midpoint_blocks():
     """bf16 rows of 16-element blocks whose amax is 3 (v_i + v_i+1) for consecutive
     E4M3 values v_i < v_i+1 (exact in bf16): with s_t = 1 the block scale
