@@ -70,6 +70,11 @@ def lib():
         L.fp8_debug_encode_e2m1_f32.argtypes = [vp, i64, vp, vp]
         L.fp8_debug_encode_f32.restype = i32
         L.fp8_debug_encode_f32.argtypes = [vp, i64, i32, vp, vp]
+        L.fp8_debug_gemm_blockscaled_wait_limit.restype = i32
+        L.fp8_debug_gemm_blockscaled_wait_limit.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp,
+                                                             u64, vp]
+        L.fp8_debug_gemm_mx_wait_limit.restype = i32
+        L.fp8_debug_gemm_mx_wait_limit.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, u64, vp]
         L.fp8_debug_wait_probe.restype = i32
         L.fp8_debug_wait_probe.argtypes = [vp, u64, vp]
         L.fp8_launch_count.restype = u64
@@ -109,6 +114,45 @@ def _check(rc: int, what: str):
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+_default_status = {}
+
+
+def default_status(device=None):
+    """The status word the GEMM wrappers pass when the caller gives none: one zeroed
+    int32 per device, allocated on first use. A bounded wait that expires inside a
+    kernel writes FP8_ERR_TIMEOUT there (the library never clears it); read it with
+    check_status() after the work has completed."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    s = _default_status.get(key)
+    if s is None:
+        s = torch.zeros(1, dtype=torch.int32, device=torch.device("cuda", key))
+        _default_status[key] = s
+    return s
+
+
+def check_status(status=None, device=None):
+    """Synchronise the device, then raise Fp8Error if a kernel recorded an error in
+    `status` (by default the per-device word the GEMM wrappers use when called
+    without one); the word is cleared afterwards. Without this check (or an
+    explicit status tensor read by the caller) a timed-out GEMM leaves its output
+    partly written and nothing reports it."""
+    import torch
+
+    s = default_status(device) if status is None else status
+    torch.cuda.synchronize(s.device)
+    code = int(s.item())
+    if code != OK:
+        s.zero_()
+        raise Fp8Error(code, "device status")
+
+
+def _status(status, t):
+    return default_status(t.device) if status is None else status
 
 
 def _stream(stream=None):
@@ -181,7 +225,11 @@ def dequantize(q, scales, fmt: int, gran: int, sf_layout: int = SF_LINEAR, out=N
 # ---------------------------------------------------------------- GEMMs
 def gemm_blockscaled(a, a_scales, a_gran: int, b, b_scales, b_gran: int, a_fmt: int = E4M3, b_fmt: int = E4M3,
                      out=None, status=None, stream=None):
-    """Out[M, N] bf16 = X_hat @ W_hat^T; a: uint8 [M, K], b: uint8 [N, K] (contiguous)."""
+    """Out[M, N] bf16 = X_hat @ W_hat^T; a: uint8 [M, K], b: uint8 [N, K] (contiguous).
+
+    status: a zeroed int32 CUDA tensor the kernel sets to ERR_TIMEOUT if a bounded
+    wait expires; None uses the per-device word of default_status(), which
+    check_status() reads. The same holds for every GEMM wrapper here."""
     import torch
 
     M, K = a.shape
@@ -189,6 +237,7 @@ def gemm_blockscaled(a, a_scales, a_gran: int, b, b_scales, b_gran: int, a_fmt: 
     assert K == K2 and a.is_contiguous() and b.is_contiguous()
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    status = _status(status, a)
     rc = lib().fp8_gemm_blockscaled(_ptr(a), _ptr(a_scales), a_gran, _ptr(b), _ptr(b_scales), b_gran, a_fmt, b_fmt,
                                     _ptr(out), M, N, K, _ptr(status), _stream(stream))
     _check(rc, "fp8_gemm_blockscaled")
@@ -210,6 +259,7 @@ def gemm_blockscaled_quantized_out(a, a_scales, b, b_scales, a_fmt: int = E4M3, 
         q_out = torch.empty((M, N), dtype=torch.uint8, device=a.device)
     if q_scales is None:
         q_scales = torch.empty((N // 128) * M, dtype=torch.float32, device=a.device)
+    status = _status(status, a)
     rc = lib().fp8_gemm_blockscaled_quantized_out(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), a_fmt, b_fmt,
                                                   out_fmt, _ptr(q_out), _ptr(q_scales), M, N, K, _ptr(status),
                                                   _stream(stream))
@@ -226,6 +276,7 @@ def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, st
     assert K == K2 and a.is_contiguous() and b.is_contiguous()
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    status = _status(status, a)
     rc = lib().fp8_gemm_mx(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), a_fmt, b_fmt, _ptr(out), M, N, K,
                            _ptr(status), _stream(stream))
     _check(rc, "fp8_gemm_mx")
@@ -282,6 +333,7 @@ def gemm_nvfp4(a, a_sf, a_ts, b, b_sf, b_ts, out=None, status=None, stream=None)
     assert Kh == Kh2 and a.is_contiguous() and b.is_contiguous()
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    status = _status(status, a)
     rc = lib().fp8_gemm_nvfp4(_ptr(a), _ptr(a_sf), _ptr(a_ts), _ptr(b), _ptr(b_sf), _ptr(b_ts), _ptr(out), M, N,
                               2 * Kh, _ptr(status), _stream(stream))
     _check(rc, "fp8_gemm_nvfp4")
@@ -308,6 +360,7 @@ def debug_gemm_blockscaled_pairs(a, a_scales, b, b_scales, a_fmt: int = E4M3, b_
     N = b.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    status = _status(status, a)
     rc = lib().fp8_debug_gemm_blockscaled_pairs(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), a_fmt, b_fmt,
                                                 _ptr(out), M, N, K, _ptr(status), _stream(stream))
     _check(rc, "fp8_debug_gemm_blockscaled_pairs")

@@ -27,6 +27,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
 bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_CHANNEL; }
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+constexpr int64_t kMaxBlockRows = int64_t{65535} * 128;  // FP8_GRAN_BLOCK_128x128
 }  // namespace
 
 int device_sm_count() {
@@ -130,8 +131,9 @@ static fp8_status_t check_quant_shape(int64_t rows, int64_t cols, int gran) {
     case FP8_GRAN_TENSOR:
     case FP8_GRAN_TOKEN:
     case FP8_GRAN_CHANNEL: return cols % 16 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
-    case FP8_GRAN_TILE_1x128:
-    case FP8_GRAN_BLOCK_128x128: return cols % 128 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
+    case FP8_GRAN_TILE_1x128: return cols % 128 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
+    // one CTA per 128 x 128 block, row blocks in gridDim.y (at most 65535)
+    case FP8_GRAN_BLOCK_128x128: return cols % 128 || rows > kMaxBlockRows ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
     case FP8_GRAN_MX32: return cols % 32 ? FP8_ERR_UNSUPPORTED_SHAPE : FP8_OK;
     default: return FP8_ERR_INVALID_ARG;
   }
@@ -227,10 +229,11 @@ static fp8_status_t check_gemm_common(const void *a, const void *b, void *out, i
   return FP8_OK;
 }
 
-fp8_status_t fp8_gemm_blockscaled(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,
-                                  const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
-                                  fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N,
-                                  int64_t K, int *dev_status, fp8_stream_t stream) {
+static fp8_status_t gemm_blockscaled_impl(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,
+                                          const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
+                                          fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M,
+                                          int64_t N, int64_t K, int *dev_status, fp8_stream_t stream,
+                                          uint64_t wait_ns, bool allow_clusters) {
   const bool fold = a_gran == FP8_GRAN_TILE_1x128 && b_gran == FP8_GRAN_BLOCK_128x128;
   const bool epi = (a_gran == FP8_GRAN_TENSOR || a_gran == FP8_GRAN_TOKEN) &&
                    (b_gran == FP8_GRAN_TENSOR || b_gran == FP8_GRAN_TOKEN);
@@ -245,10 +248,20 @@ fp8_status_t fp8_gemm_blockscaled(const void *a_dev, const float *a_scales_dev, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (fold)
     return launch_gemm_fold(static_cast<const uint8_t *>(a_dev), a_scales_dev, static_cast<const uint8_t *>(b_dev),
-                            b_scales_dev, a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status, s);
+                            b_scales_dev, a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status, s,
+                            wait_ns, allow_clusters);
   return launch_gemm_epilogue_scaled(static_cast<const uint8_t *>(a_dev), a_scales_dev, a_gran == FP8_GRAN_TOKEN,
                                      static_cast<const uint8_t *>(b_dev), b_scales_dev, b_gran == FP8_GRAN_TOKEN,
-                                     a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status, s);
+                                     a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status, s,
+                                     wait_ns);
+}
+
+fp8_status_t fp8_gemm_blockscaled(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,
+                                  const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
+                                  fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N,
+                                  int64_t K, int *dev_status, fp8_stream_t stream) {
+  return gemm_blockscaled_impl(a_dev, a_scales_dev, a_gran, b_dev, b_scales_dev, b_gran, a_fmt, b_fmt, out_dev, M, N,
+                               K, dev_status, stream, kWaitTimeoutNs, true);
 }
 
 fp8_status_t fp8_gemm_blockscaled_quantized_out(const void *a_dev, const float *a_scales_dev, const void *b_dev,
@@ -269,9 +282,10 @@ fp8_status_t fp8_gemm_blockscaled_quantized_out(const void *a_dev, const float *
                                     reinterpret_cast<cudaStream_t>(stream));
 }
 
-fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
-                         fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
-                         int *dev_status, fp8_stream_t stream) {
+static fp8_status_t gemm_mx_impl(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                 const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev,
+                                 int64_t M, int64_t N, int64_t K, int *dev_status, fp8_stream_t stream,
+                                 uint64_t wait_ns) {
   fp8_status_t st = check_gemm_common(a_dev, b_dev, out_dev, M, N, K, a_fmt, b_fmt);
   if (st != FP8_OK || M == 0 || N == 0) return st;
   if (K % 32) return FP8_ERR_UNSUPPORTED_SHAPE;
@@ -280,7 +294,33 @@ fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void 
   if (dev_status != nullptr && !aligned(dev_status, 4)) return FP8_ERR_ALIGNMENT;
   return launch_gemm_mx(static_cast<const uint8_t *>(a_dev), a_sf_dev, static_cast<const uint8_t *>(b_dev), b_sf_dev,
                         a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status,
-                        reinterpret_cast<cudaStream_t>(stream));
+                        reinterpret_cast<cudaStream_t>(stream), wait_ns);
+}
+
+fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
+                         fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
+                         int *dev_status, fp8_stream_t stream) {
+  return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
+                      kWaitTimeoutNs);
+}
+
+fp8_status_t fp8_debug_gemm_blockscaled_wait_limit(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,
+                                                   const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
+                                                   fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M,
+                                                   int64_t N, int64_t K, int *dev_status, uint64_t wait_ns,
+                                                   fp8_stream_t stream) {
+  if (dev_status == nullptr || wait_ns == 0 || wait_ns > 10000000000ull) return FP8_ERR_INVALID_ARG;
+  return gemm_blockscaled_impl(a_dev, a_scales_dev, a_gran, b_dev, b_scales_dev, b_gran, a_fmt, b_fmt, out_dev, M, N,
+                               K, dev_status, stream, wait_ns, false);
+}
+
+fp8_status_t fp8_debug_gemm_mx_wait_limit(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                          const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt,
+                                          void *out_dev, int64_t M, int64_t N, int64_t K, int *dev_status,
+                                          uint64_t wait_ns, fp8_stream_t stream) {
+  if (dev_status == nullptr || wait_ns == 0 || wait_ns > 10000000000ull) return FP8_ERR_INVALID_ARG;
+  return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
+                      wait_ns);
 }
 
 size_t fp8_nvfp4_scales_bytes(int64_t rows, int64_t cols, fp8_sf_layout_t sf_layout) {

@@ -114,10 +114,6 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
 #define FOLD_MMA_ISSUERS 2  // threads (in warps 1..) issuing the fold kernels' MMAs, k-blocks dealt round robin
 #endif
 
-#ifndef FOLD_SCALE_AHEAD
-#define FOLD_SCALE_AHEAD 2  // k-blocks between a fold's scale loads and their use
-#endif
-
 #ifndef FOLD_CHUNK
 #define FOLD_CHUNK 64  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
 #endif
@@ -212,7 +208,8 @@ bool reg_split_fits(KernelT kernel, int threads, uint32_t needed) {
 
 // Epilogue through shared memory and TMA stores. The warp's 32 rows x 128
 // columns leave as boxes 128 bytes wide and 32 rows high (bf16: two boxes of 64
-// columns; fp8 codes: one box of 128 columns), each written into one of the
+// columns, the first at column n0 and the second at n1; fp8 codes: one box of
+// 128 columns at n0), each written into one of the
 // warp's NSLOTS 4 KB staging slots in the 128-byte swizzled layout of the
 // output tensor map (16-byte chunk c of row r at chunk c ^ (r % 8)). Lane 0
 // issues the stores and returns at once; a slot is rewritten only after the
@@ -222,8 +219,8 @@ bool reg_split_fits(KernelT kernel, int threads, uint32_t needed) {
 // memory (the caller issues the next tile's first scale loads there, so their
 // latency hides behind the rest of the epilogue).
 template <int QFMT, int NSLOTS, int NA, typename Mid>
-__device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[NA], int m, int row0, int n0, int M, int N,
-                                                  const CUtensorMap *tmo, uint8_t *slots, float *q_scales,
+__device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[NA], int m, int row0, int n0, int n1, int M,
+                                                  int N, const CUtensorMap *tmo, uint8_t *slots, float *q_scales,
                                                   int lane, Mid &&mid) {
   static_assert(NA == 32 || NA == 64, "32 or 64 column pairs per thread");
   static_assert(QFMT < 0 || NA == 64, "the quantized output needs a whole 1x128 group per thread");
@@ -250,8 +247,9 @@ __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[NA], int m, int 
             make_uint4(p[32 * bx + 4 * c], p[32 * bx + 4 * c + 1], p[32 * bx + 4 * c + 2], p[32 * bx + 4 * c + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && rows_in && n0 + 64 * bx < N) {
-        tma_store_2d(tmo, slots + (bx % NSLOTS) * 4096, n0 + 64 * bx, row0);
+      const int nb = bx == 0 ? n0 : n1;
+      if (lane == 0 && rows_in && nb < N) {
+        tma_store_2d(tmo, slots + (bx % NSLOTS) * 4096, nb, row0);
         bulk_commit_group();
       }
       if (bx == 0) mid();
@@ -299,7 +297,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
     gemm_fold_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const float *__restrict__ sa,
                      const float *__restrict__ sb, float *__restrict__ q_scales, int M, int N, int K, uint32_t idesc,
-                     int *dev_status, int group_m) {
+                     int *dev_status, int group_m, uint64_t wait_ns) {
   using C = FoldCfg<BN, STAGES, NBUF>;
   constexpr int ISSUERS = FOLD_MMA_ISSUERS;
   static_assert(ISSUERS >= 1 && ISSUERS <= 3 && NBUF % ISSUERS == 0, "each partial buffer needs one issuer");
@@ -356,7 +354,7 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
         tile_coords(tile, num_m, num_n, group_m, mt, nt);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
-          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -388,8 +386,8 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
           // the stage's operands first (they usually landed long before), then
           // the partial buffer: the fold's release is the critical path, and a
           // wait on an already completed barrier still costs ~100 cycles
-          if (!mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort) ||
-              !mbar_wait(&tempty[b], ((kc / NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, wait_ns, &ctl.abort) ||
+              !mbar_wait(&tempty[b], ((kc / NBUF) & 1) ^ 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -416,60 +414,61 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
     int kc = 0;
     bool ok = true;
     float2 acc[WC / 2];
-    // Scales are loaded SA k-blocks ahead of their fold (a register ring); the
-    // first SA pairs of a tile are loaded in the previous tile's epilogue (see
-    // fold_epilogue_tma), else at the top of the tile.
-    constexpr int SA = FOLD_SCALE_AHEAD;
-    auto first_scales = [&](int t, float (&a)[SA], float (&b)[SA]) {
+    // Scales: each k-block's pair (s_x of this thread's row, s_w of its slab's
+    // weight block) is loaded two k-blocks before its fold into one of two
+    // register slots, and the slot is reloaded right after it is read. The
+    // k-block loop runs in pairs so that each slot is a fixed register: no
+    // register copy ever waits on a load in flight (a shifted ring of loaded
+    // values stalls every k-block for a whole global-load latency). Indices are
+    // clamped instead of predicated, so no select consumes a load either: a
+    // clamped load only feeds rows or k-blocks that are never stored.
+    // The first two pairs of a tile are loaded during the previous tile's
+    // epilogue (see fold_epilogue_tma), else at the top of the tile.
+    auto first_scales = [&](int t, float &a0, float &b0, float &a1, float &b1) {
       int tm, tn;
       tile_coords(t, num_m, num_n, group_m, tm, tn);
-      const int tr = tm * BM + quarter * 32 + lane;
-      const int tb = (tn * BN + half * WC) / 128;
+      const int tr = min(tm * BM + quarter * 32 + lane, M - 1);
+      const int tb = min((tn * BN + half * WC) / 128, nblk128 - 1);
       const float *pa = sa + tr;
       const float *pb = sb + static_cast<int64_t>(tb) * KB;
-#pragma unroll
-      for (int j = 0; j < SA; ++j) {
-        a[j] = (tr < M && j < KB) ? __ldg(pa + static_cast<int64_t>(j) * M) : 0.0f;
-        b[j] = (tb < nblk128 && j < KB) ? __ldg(pb + j) : 0.0f;
-      }
+      const int k1 = KB > 1 ? 1 : 0;
+      a0 = __ldg(pa);
+      b0 = __ldg(pb);
+      a1 = __ldg(pa + static_cast<int64_t>(k1) * M);
+      b1 = __ldg(pb + k1);
     };
-    float nsa[SA], nsb[SA];
+    float nsa0 = 0.0f, nsb0 = 0.0f, nsa1 = 0.0f, nsb1 = 0.0f;
     bool have_next = false;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, num_m, num_n, group_m, mt, nt);
       const int m = mt * BM + quarter * 32 + lane;
-      const bool row_ok = m < M;
       const int nb = (nt * BN + half * WC) / 128;  // weight block of this slab
-      const bool col_ok = nb < nblk128;
-      const float *sa_row = sa + m;
-      const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
+      const float *sa_row = sa + min(m, M - 1);
+      const float *sb_blk = sb + static_cast<int64_t>(min(nb, nblk128 - 1)) * KB;
 #pragma unroll
       for (int i = 0; i < WC / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      // scales of k-blocks kb .. kb + SA - 1
-      float sa_ring[SA], sb_ring[SA];
+      float sa0, sb0, sa1, sb1;  // slot 0: even k-blocks, slot 1: odd k-blocks
       if (have_next) {
-#pragma unroll
-        for (int j = 0; j < SA; ++j) {
-          sa_ring[j] = nsa[j];
-          sb_ring[j] = nsb[j];
-        }
+        sa0 = nsa0;
+        sb0 = nsb0;
+        sa1 = nsa1;
+        sb1 = nsb1;
       } else {
-        first_scales(tile, sa_ring, sb_ring);
+        first_scales(tile, sa0, sb0, sa1, sb1);
       }
-      for (int kb = 0; kb < KB; ++kb, ++kc) {
+      // fold k-block kb with the scales in (sa_s, sb_s), then reload that slot for kb + 2
+      auto fold_one = [&](int kb, float &sa_s, float &sb_s) -> bool {
         const int b = kc % NBUF;
-        const float sa_next = (row_ok && kb + SA < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + SA) * M) : 0.0f;
-        const float sb_next = (col_ok && kb + SA < KB) ? __ldg(sb_blk + kb + SA) : 0.0f;
-        const float sc = sa_ring[0] * sb_ring[0];
+        const float sc = sa_s * sb_s;
         const float2 sc2 = make_float2(sc, sc);
+        const int kn = min(kb + 2, KB - 1);
+        sa_s = __ldg(sa_row + static_cast<int64_t>(kn) * M);
+        sb_s = __ldg(sb_blk + kn);
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BN + half * WC);
         // every lane polls (one polling lane and a broadcast measured 7 % slower)
-        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, wait_ns, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) return false;
         tc_fence_after();
         constexpr int CH = FOLD_CHUNK < WC ? FOLD_CHUNK : WC, NCH = WC / CH;
         if constexpr (CH >= 64) {
@@ -507,21 +506,21 @@ __global__ void __launch_bounds__(FoldCfg<BN, STAGES, NBUF>::THREADS, 1)
             }
           }
         }
-#pragma unroll
-        for (int j = 0; j + 1 < SA; ++j) {
-          sa_ring[j] = sa_ring[j + 1];
-          sb_ring[j] = sb_ring[j + 1];
-        }
-        sa_ring[SA - 1] = sa_next;
-        sb_ring[SA - 1] = sb_next;
+        ++kc;
+        return true;
+      };
+      for (int kb = 0; kb < KB && ok; kb += 2) {
+        ok = fold_one(kb, sa0, sb0);
+        if (ok && kb + 1 < KB) ok = fold_one(kb + 1, sa1, sb1);
       }
       if (!ok) break;
       const int next = tile + static_cast<int>(gridDim.x);
-      fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * BM + quarter * 32, nt * BN + half * WC, M, N, &tmO,
+      fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * BM + quarter * 32, nt * BN + half * WC,
+                                            nt * BN + half * WC + 64, M, N, &tmO,
                                             smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
                                             lane, [&]() {
                                               have_next = next < ntiles;
-                                              if (have_next) first_scales(next, nsa, nsb);
+                                              if (have_next) first_scales(next, nsa0, nsb0, nsa1, nsb1);
                                             });
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
@@ -693,18 +692,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
     int kc = 0;
     bool ok = true;
     float2 acc[64];
-    // first two scale pairs of a tile, as in the single-CTA kernel
+    // first two scale pairs of a tile, in two fixed register slots reloaded in
+    // place with clamped indices, as in the single-CTA kernel
     auto first_scales = [&](int t, float &a0, float &b0, float &a1, float &b1) {
       int tm, tn;
       tile_coords(t, num_m, num_n, group_m, tm, tn);
-      const int tr = tm * C::TM + static_cast<int>(rank) * 128 + quarter * 32 + lane;
-      const int tb = tn * 2 + half;
+      const int tr = min(tm * C::TM + static_cast<int>(rank) * 128 + quarter * 32 + lane, M - 1);
+      const int tb = min(tn * 2 + half, nblk128 - 1);
       const float *pa = sa + tr;
       const float *pb = sb + static_cast<int64_t>(tb) * KB;
-      a0 = tr < M ? __ldg(pa) : 0.0f;
-      b0 = tb < nblk128 ? __ldg(pb) : 0.0f;
-      a1 = (tr < M && KB > 1) ? __ldg(pa + static_cast<int64_t>(M)) : 0.0f;
-      b1 = (tb < nblk128 && KB > 1) ? __ldg(pb + 1) : 0.0f;
+      const int k1 = KB > 1 ? 1 : 0;
+      a0 = __ldg(pa);
+      b0 = __ldg(pb);
+      a1 = __ldg(pa + static_cast<int64_t>(k1) * M);
+      b1 = __ldg(pb + k1);
     };
     float nsa0 = 0.0f, nsb0 = 0.0f, nsa1 = 0.0f, nsb1 = 0.0f;
     bool have_next = false;
@@ -712,11 +713,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
       int mt, nt;
       tile_coords(tile, num_m, num_n, group_m, mt, nt);
       const int m = mt * C::TM + static_cast<int>(rank) * 128 + quarter * 32 + lane;
-      const bool row_ok = m < M;
       const int nb = nt * 2 + half;
-      const bool col_ok = nb < nblk128;
-      const float *sa_row = sa + m;
-      const float *sb_blk = sb + static_cast<int64_t>(nb) * KB;
+      const float *sa_row = sa + min(m, M - 1);
+      const float *sb_blk = sb + static_cast<int64_t>(min(nb, nblk128 - 1)) * KB;
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
       float sa0, sb0, sa1, sb1;
@@ -728,18 +727,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
       } else {
         first_scales(tile, sa0, sb0, sa1, sb1);
       }
-      for (int kb = 0; kb < KB; ++kb, ++kc) {
+      auto fold_one = [&](int kb, float &sa_s, float &sb_s) -> bool {
         const int b = kc & 1;
-        const float sa2 = (row_ok && kb + 2 < KB) ? __ldg(sa_row + static_cast<int64_t>(kb + 2) * M) : 0.0f;
-        const float sb2 = (col_ok && kb + 2 < KB) ? __ldg(sb_blk + kb + 2) : 0.0f;
-        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float sc = sa0 * sb0;
+        const float sc = sa_s * sb_s;
         const float2 sc2 = make_float2(sc, sc);
+        const int kn = min(kb + 2, KB - 1);
+        sa_s = __ldg(sa_row + static_cast<int64_t>(kn) * M);
+        sb_s = __ldg(sb_blk + kn);
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        tc_fence_after();
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * C::TN + half * 128);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -754,15 +751,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
           }
           fold_chunk<64>(acc, c * 32, sc2, rb);
         }
-        sa0 = sa1;
-        sb0 = sb1;
-        sa1 = sa2;
-        sb1 = sb2;
+        ++kc;
+        return true;
+      };
+      for (int kb = 0; kb < KB && ok; kb += 2) {
+        ok = fold_one(kb, sa0, sb0);
+        if (ok && kb + 1 < KB) ok = fold_one(kb + 1, sa1, sb1);
       }
       if (!ok) break;
       const int next = tile + npairs;
       fold_epilogue_tma<QFMT, C::EPI_SLOTS>(acc, m, mt * C::TM + static_cast<int>(rank) * 128 + quarter * 32,
-                                            nb * 128, M, N, &tmO,
+                                            nb * 128, nb * 128 + 64, M, N, &tmO,
                                             smem + STAGES * C::STAGE_BYTES + cw * C::EPI_SLOTS * 4096, q_scales,
                                             lane, [&]() {
                                               have_next = next < ntiles;
@@ -805,7 +804,7 @@ template <int BX, int STAGES>
 __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
     gemm_fold_swap_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                           const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
-                          int M, int N, int K, uint32_t idesc, int *dev_status) {
+                          int M, int N, int K, uint32_t idesc, int *dev_status, uint64_t wait_ns) {
   using C = SwapCfg<BX, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -856,7 +855,7 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         const int wt = tile / num_x, xt = tile - wt * num_x;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
-          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -884,8 +883,8 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
           const uint32_t d = tmem + static_cast<uint32_t>(b * BX);
           // the partial buffer (usually free) before the stage (the copy in
           // flight from HBM is the critical wait); descriptors formed first
-          if (!mbar_wait(&tempty[b], ((kc / C::NBUF) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort) ||
-              !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (!mbar_wait(&tempty[b], ((kc / C::NBUF) & 1) ^ 1, wait_ns, &ctl.abort) ||
+              !mbar_wait(&full[s], (it / STAGES) & 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -913,27 +912,30 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
 #pragma unroll
       for (int j = 0; j < BX; ++j) acc[j] = 0.0f;
-      // lane l holds s_x[kb, m0 + 32 r + l]; prefetched two chunks ahead
-      float x0[XR], x1[XR], x2[XR];
+      // lane l holds s_x[kb, m0 + 32 r + l] and s_w[kb] in one of two fixed
+      // register slots (even / odd k-blocks), loaded two k-blocks ahead and
+      // reloaded in place; indices are clamped, not predicated, so that no copy
+      // or select waits on a load in flight (values of rows past M are never stored)
       auto load_sx = [&](int kbq, float (&dst)[XR]) {
+        const int kq = min(kbq, KB - 1);
 #pragma unroll
-        for (int r = 0; r < XR; ++r) {
-          const int mm = m0 + 32 * r + lane;
-          dst[r] = (kbq < KB && 32 * r + lane < BX && mm < M) ? __ldg(sa + static_cast<int64_t>(kbq) * M + mm) : 0.0f;
-        }
+        for (int r = 0; r < XR; ++r) dst[r] = __ldg(sa + static_cast<int64_t>(kq) * M + min(m0 + 32 * r + lane, M - 1));
       };
-      load_sx(0, x0);
-      load_sx(1, x1);
-      float w0 = __ldg(sb_blk), w1 = KB > 1 ? __ldg(sb_blk + 1) : 0.0f;
-      for (int kb = 0; kb < KB; ++kb, ++kc) {
+      float xs0[XR], xs1[XR];
+      load_sx(0, xs0);
+      load_sx(1, xs1);
+      float ws0 = __ldg(sb_blk), ws1 = __ldg(sb_blk + (KB > 1 ? 1 : 0));
+      auto fold_one = [&](int kb, float (&xs)[XR], float &ws) -> bool {
         const int b = kc % C::NBUF;
-        load_sx(kb + 2, x2);
-        const float w2 = kb + 2 < KB ? __ldg(sb_blk + kb + 2) : 0.0f;
-        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
+        // lane l forms s_w * s_x for activation rows l (+ 32 r) once; the
+        // shuffles then carry finished products (same fp32 multiply)
+        float cs[XR];
+#pragma unroll
+        for (int q = 0; q < XR; ++q) cs[q] = ws * xs[q];
+        load_sx(kb + 2, xs);
+        ws = __ldg(sb_blk + min(kb + 2, KB - 1));
+        const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, wait_ns, &ctl.abort);
+        if (!__all_sync(0xffffffffu, got)) return false;
         tc_fence_after();
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
         // the whole BX-column partial in one load and one wait
@@ -943,23 +945,17 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
-        // lane l forms s_w * s_x for activation rows l (+ 32 r) once; the
-        // shuffles then carry finished products (same fp32 multiply)
-        float cs[XR];
-#pragma unroll
-        for (int q = 0; q < XR; ++q) cs[q] = w0 * x0[q];
 #pragma unroll
         for (int j = 0; j < BX; ++j) {
           const float sc = __shfl_sync(0xffffffffu, cs[j / 32], j % 32);
           acc[j] = fmaf(sc, __uint_as_float(r[j]), acc[j]);
         }
-#pragma unroll
-        for (int r = 0; r < XR; ++r) {
-          x0[r] = x1[r];
-          x1[r] = x2[r];
-        }
-        w0 = w1;
-        w1 = w2;
+        ++kc;
+        return true;
+      };
+      for (int kb = 0; kb < KB && ok; kb += 2) {
+        ok = fold_one(kb, xs0, ws0);
+        if (ok && kb + 1 < KB) ok = fold_one(kb + 1, xs1, ws1);
       }
       if (!ok) break;
       if (n < N) {
@@ -1126,27 +1122,25 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
       const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
 #pragma unroll
       for (int j = 0; j < BX; ++j) acc[j] = 0.0f;
-      // lane l holds s_x[kb, m0 + 32 r + l]; prefetched two chunks ahead
-      float x0[XR], x1[XR], x2[XR];
+      // scale slots as in the unsplit kernel, over this CTA's k-blocks [kb_lo, kb_hi)
       auto load_sx = [&](int kbq, float (&dst)[XR]) {
+        const int kq = min(kbq, kb_hi - 1);
 #pragma unroll
-        for (int r = 0; r < XR; ++r) {
-          const int mm = m0 + 32 * r + lane;
-          dst[r] = (kbq < kb_hi && 32 * r + lane < BX && mm < M) ? __ldg(sa + static_cast<int64_t>(kbq) * M + mm) : 0.0f;
-        }
+        for (int r = 0; r < XR; ++r) dst[r] = __ldg(sa + static_cast<int64_t>(kq) * M + min(m0 + 32 * r + lane, M - 1));
       };
-      load_sx(kb_lo, x0);
-      load_sx(kb_lo + 1, x1);
-      float w0 = __ldg(sb_blk + kb_lo), w1 = kb_lo + 1 < kb_hi ? __ldg(sb_blk + kb_lo + 1) : 0.0f;
-      for (int kb = kb_lo; kb < kb_hi; ++kb, ++kc) {
+      float xs0[XR], xs1[XR];
+      load_sx(kb_lo, xs0);
+      load_sx(kb_lo + 1, xs1);
+      float ws0 = __ldg(sb_blk + kb_lo), ws1 = __ldg(sb_blk + min(kb_lo + 1, kb_hi - 1));
+      auto fold_one = [&](int kb, float (&xs)[XR], float &ws) -> bool {
         const int b = kc % C::NBUF;
-        load_sx(kb + 2, x2);
-        const float w2 = kb + 2 < kb_hi ? __ldg(sb_blk + kb + 2) : 0.0f;
+        float cs[XR];
+#pragma unroll
+        for (int q = 0; q < XR; ++q) cs[q] = ws * xs[q];
+        load_sx(kb + 2, xs);
+        ws = __ldg(sb_blk + min(kb + 2, kb_hi - 1));
         const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
+        if (!__all_sync(0xffffffffu, got)) return false;
         tc_fence_after();
         const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
         // the whole BX-column partial in one load and one wait
@@ -1156,23 +1150,17 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
-        // lane l forms s_w * s_x for activation rows l (+ 32 r) once; the
-        // shuffles then carry finished products (same fp32 multiply)
-        float cs[XR];
-#pragma unroll
-        for (int q = 0; q < XR; ++q) cs[q] = w0 * x0[q];
 #pragma unroll
         for (int j = 0; j < BX; ++j) {
           const float sc = __shfl_sync(0xffffffffu, cs[j / 32], j % 32);
           acc[j] = fmaf(sc, __uint_as_float(r[j]), acc[j]);
         }
-#pragma unroll
-        for (int r = 0; r < XR; ++r) {
-          x0[r] = x1[r];
-          x1[r] = x2[r];
-        }
-        w0 = w1;
-        w1 = w2;
+        ++kc;
+        return true;
+      };
+      for (int kb = kb_lo; kb < kb_hi && ok; kb += 2) {
+        ok = fold_one(kb, xs0, ws0);
+        if (ok && kb + 1 < kb_hi) ok = fold_one(kb + 1, xs1, ws1);
       }
       if (!ok) break;
       {
@@ -1295,7 +1283,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
     gemm_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float *__restrict__ sa, int sa_per_row, const float *__restrict__ sb, int sb_per_col,
                      const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb, uint16_t *__restrict__ out,
-                     int M, int N, int K, uint32_t idesc, int *dev_status, int group_m) {
+                     int M, int N, int K, uint32_t idesc, int *dev_status, int group_m, uint64_t wait_ns) {
   using C = AccCfg<KIND, BN, STAGES, NACC>;
   constexpr bool MX = C::MX;
   constexpr bool F4 = KIND == KIND_NVF4;
@@ -1353,7 +1341,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
         tile_coords(tile, num_m, num_n, group_m, mt, nt);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
-          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -1402,7 +1390,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           const uint64_t sf_desc = sdesc_plain_32x16(smem_u32(smem + s * C::STAGE_STRIDE) + C::A_BYTES + C::B_BYTES);
-          if (!mbar_wait(C::SF_SPLIT ? &sf_full[s] : &full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (!mbar_wait(C::SF_SPLIT ? &sf_full[s] : &full[s], (it / STAGES) & 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -1423,7 +1411,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
       const uint32_t sf_col0 = static_cast<uint32_t>(C::ACC_COLS);
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tc) {
         const int b = tc % NACC;
-        if (!mbar_wait(&aempty[b], ((tc / NACC) & 1) ^ 1, kWaitTimeoutNs, &ctl.abort)) {
+        if (!mbar_wait(&aempty[b], ((tc / NACC) & 1) ^ 1, wait_ns, &ctl.abort)) {
           ok = false;
           break;
         }
@@ -1438,11 +1426,11 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
           const uint64_t adesc = sdesc_k_sw128(a0), bdesc = sdesc_k_sw128(b0);
           // the operands, and (block-scaled kinds) the scale atoms in tensor
           // memory; without SF_SPLIT sf_ready[s] implies full[s]
-          if ((!C::COPIER || C::SF_SPLIT) && !mbar_wait(&full[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+          if ((!C::COPIER || C::SF_SPLIT) && !mbar_wait(&full[s], (it / STAGES) & 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
-          if (C::COPIER && !mbar_wait(&sf_ready[s], (it / STAGES) & 1, kWaitTimeoutNs, &ctl.abort)) {
+          if (C::COPIER && !mbar_wait(&sf_ready[s], (it / STAGES) & 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
           }
@@ -1498,7 +1486,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
       const int m = mt * BM + quarter * 32 + lane;
       const bool row_ok = m < M;
       const int n0 = nt * BN + half * 128;
-      const bool got = mbar_wait(&afull[b], (tc / NACC) & 1, kWaitTimeoutNs, &ctl.abort);
+      const bool got = mbar_wait(&afull[b], (tc / NACC) & 1, wait_ns, &ctl.abort);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -1646,14 +1634,14 @@ int swap_split(int64_t units, int64_t KB, int sms, int capacity) {
 template <int BX, int ST>
 fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, uint64_t wait_ns, bool allow_clusters) {
   CUtensorMap tx, tw;
   if (!make_tmap_u8(&tx, a, M, K, K, BX, BK) || !make_tmap_u8(&tw, b, N, K, K, BM, BK)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + BX - 1) / BX) * ((N + BM - 1) / BM));
   // the MMA's A operand is W (format b_fmt), its B operand is X (a_fmt)
   const uint32_t idesc = idesc_f8f6f4(b_fmt, a_fmt, BM, BX);
   const int sms = device_sm_count();
-  if (ntiles * 10 < sms * 9 && K / BK >= 4) {
+  if (allow_clusters && ntiles * 10 < sms * 9 && K / BK >= 4) {
     // split-K clusters; 5 stages (the fewest the stage-barrier parity allows)
     // so that two CTAs fit on an SM where registers allow
     constexpr int STS = 5;
@@ -1688,8 +1676,8 @@ fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *
   auto kern = gemm_fold_swap_kernel<BX, ST>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, tx, tw,
-                       sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), idesc,
-                       dev_status) != cudaSuccess)
+                       sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), idesc, dev_status,
+                       wait_ns) != cudaSuccess)
     return FP8_ERR_CUDA;
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
@@ -1728,7 +1716,7 @@ bool use_pairs(int64_t M, int64_t N) {
 template <int BN, int ST, int NBUF, int QFMT>
 fp8_status_t launch_fold_cfg(const CUtensorMap &ta, const CUtensorMap &to, const uint8_t *b, const float *sa,
                              const float *sb, float *q_scales, int a_fmt, int b_fmt, int64_t M, int64_t N, int64_t K,
-                             int *dev_status, cudaStream_t stream) {
+                             int *dev_status, cudaStream_t stream, uint64_t wait_ns) {
   using C = FoldCfg<BN, ST, NBUF>;
   CUtensorMap tb;
   if (!make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
@@ -1737,7 +1725,7 @@ fp8_status_t launch_fold_cfg(const CUtensorMap &ta, const CUtensorMap &to, const
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, ta, tb, to,
                        sa, sb, q_scales, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                       idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K)) != cudaSuccess)
+                       idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K), wait_ns) != cudaSuccess)
     return FP8_ERR_CUDA;
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
@@ -1746,7 +1734,7 @@ fp8_status_t launch_fold_cfg(const CUtensorMap &ta, const CUtensorMap &to, const
 template <int QFMT>
 fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                                int b_fmt, uint16_t *out, uint8_t *q_out, float *q_scales, int64_t M, int64_t N,
-                               int64_t K, int *dev_status, cudaStream_t stream) {
+                               int64_t K, int *dev_status, cudaStream_t stream, uint64_t wait_ns = kWaitTimeoutNs) {
   CUtensorMap ta, to;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK)) return FP8_ERR_CUDA;
   // output boxes: 32 rows x 128 bytes (bf16: 64 columns; fp8 codes: 128)
@@ -1755,14 +1743,16 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
   if constexpr (QFMT < 0 && FOLD_BF16_BN == 128) {
     // 128-wide tiles, four partial buffers: the MMA runs up to four k-blocks
     // ahead of the fold
-    return launch_fold_cfg<128, 6, 4, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K, dev_status, stream);
+    return launch_fold_cfg<128, 6, 4, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K, dev_status, stream,
+                                            wait_ns);
   } else {
     // Wide tiles when there are enough of them to fill the GPU, else 128-wide.
     const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
     if (tiles256 >= device_sm_count())
       return launch_fold_cfg<256, FOLD_WIDE_STAGES, 2, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K,
-                                                             dev_status, stream);
-    return launch_fold_cfg<128, 6, 2, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K, dev_status, stream);
+                                                             dev_status, stream, wait_ns);
+    return launch_fold_cfg<128, 6, 2, QFMT>(ta, to, b, sa, sb, q_scales, a_fmt, b_fmt, M, N, K, dev_status, stream,
+                                            wait_ns);
   }
 }
 
@@ -1770,15 +1760,22 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
 
 fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, uint64_t wait_ns, bool allow_clusters) {
   // Few activation rows (decode): swap operands so the 128-row MMA side is W.
   // 8-stage rings (5 to 12 stages measured the same or slower)
-  if (M <= 16) return launch_fold_swap<16, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
-  if (M <= 32) return launch_fold_swap<32, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
-  if (M <= 64) return launch_fold_swap<64, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream);
-  if (use_pairs(M, N))
+  if (M <= 16)
+    return launch_fold_swap<16, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream, wait_ns,
+                                   allow_clusters);
+  if (M <= 32)
+    return launch_fold_swap<32, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream, wait_ns,
+                                   allow_clusters);
+  if (M <= 64)
+    return launch_fold_swap<64, 8>(a, sa, b, sb, a_fmt, b_fmt, out, M, N, K, dev_status, stream, wait_ns,
+                                   allow_clusters);
+  if (allow_clusters && use_pairs(M, N))
     return launch_fold_pairs<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
-  return launch_fold_tiles<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream);
+  return launch_fold_tiles<-1>(a, sa, b, sb, a_fmt, b_fmt, out, nullptr, nullptr, M, N, K, dev_status, stream,
+                               wait_ns);
 }
 
 // The CTA-pair fold kernel regardless of the shape rule (M >= 1): for its tests.
@@ -1807,7 +1804,8 @@ fp8_status_t launch_gemm_fold_quantized(const uint8_t *a, const float *sa, const
 
 fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool a_token, const uint8_t *b,
                                          const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,
-                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream) {
+                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream,
+                                         uint64_t wait_ns) {
   constexpr int BN = 256, ST = 4, NACC = 2;
   using C = AccCfg<KIND_EPI, BN, ST, NACC>;
   CUtensorMap ta, tb;
@@ -1817,14 +1815,15 @@ fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
       ta, tb, sa, a_token ? 1 : 0, sb, b_token ? 1 : 0, nullptr, nullptr, out, static_cast<int>(M),
-      static_cast<int>(N), static_cast<int>(K), idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K));
+      static_cast<int>(N), static_cast<int>(K), idesc_f8f6f4(a_fmt, b_fmt, BM, BN), dev_status, raster_group(M, K),
+      wait_ns);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb, int a_fmt,
                             int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, uint64_t wait_ns) {
   constexpr int BN = MX_BN, ST = MX_STAGES, NACC = MX_NACC;
   using C = AccCfg<KIND_MX8, BN, ST, NACC>;
   CUtensorMap ta, tb;
@@ -1834,7 +1833,7 @@ fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t 
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
       ta, tb, nullptr, 0, nullptr, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-      idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status, raster_group(M, K));
+      idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status, raster_group(M, K), wait_ns);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -1856,7 +1855,7 @@ fp8_status_t launch_gemm_nvfp4(const uint8_t *a, const uint8_t *sfa, const float
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
   kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
       tma, tmb, ta, 0, tb, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-      idesc_mxf4nvf4(BM, BN), dev_status, raster_group(M, kbytes));
+      idesc_mxf4nvf4(BM, BN), dev_status, raster_group(M, kbytes), kWaitTimeoutNs);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }

@@ -44,9 +44,12 @@ fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int
 // ----------------------------------------------------------------- GEMMs
 enum class EpiScale : int { kTensorTensor = 0, kTensorToken = 1, kTokenTensor = 2, kTokenToken = 3 };
 
+// wait_ns: the kernels' bounded-wait limit (kWaitTimeoutNs in production; the
+// timeout-exit check passes a short one). allow_clusters = false keeps to the
+// single-CTA kernels (no CTA-pair or split-K cluster kernel).
 fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
-                              cudaStream_t stream);
+                              cudaStream_t stream, uint64_t wait_ns = kWaitTimeoutNs, bool allow_clusters = true);
 
 fp8_status_t launch_gemm_fold_pairs(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                                     int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
@@ -57,11 +60,12 @@ fp8_status_t launch_gemm_fold_quantized(const uint8_t *a, const float *sa, const
 
 fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool a_token, const uint8_t *b,
                                          const float *sb, bool b_token, int a_fmt, int b_fmt, uint16_t *out,
-                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream);
+                                         int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream,
+                                         uint64_t wait_ns = kWaitTimeoutNs);
 
 fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb, int a_fmt,
                             int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
-                            cudaStream_t stream);
+                            cudaStream_t stream, uint64_t wait_ns = kWaitTimeoutNs);
 
 fp8_status_t launch_wait_probe(int *dev_status, uint64_t timeout_ns, cudaStream_t stream);
 

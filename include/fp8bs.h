@@ -127,7 +127,9 @@ size_t fp8_quantize_workspace_bytes(int64_t rows, int64_t cols, fp8_gran_t gran)
  *                (may be NULL when that is 0); its contents are clobbered;
  *                concurrent calls must not share it.
  * Shape rules: cols % 16 == 0 (TENSOR, TOKEN, CHANNEL), cols % 128 == 0 (TILE_1x128,
- * BLOCK_128x128), cols % 32 == 0 (MX32). x_dev and q_dev 16-byte aligned,
+ * BLOCK_128x128), cols % 32 == 0 (MX32); rows <= 65535 * 128 for BLOCK_128x128
+ * (one CTA per block, row blocks in the grid's y dimension); other dimensions
+ * below 2^31. x_dev and q_dev 16-byte aligned,
  * ld_x % 8 == 0, ld_q % 16 == 0, scales_dev 4-byte aligned. */
 fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t ld_x, fp8_format_t fmt,
                           fp8_gran_t gran, fp8_sf_layout_t sf_layout, const float *static_scale_dev, void *q_dev,
@@ -320,6 +322,25 @@ fp8_status_t fp8_debug_encode_e2m1_f32(const float *x_dev, int64_t n, void *out_
  * FP8_ERR_TIMEOUT into *dev_status and returns, leaving the context usable.
  * timeout_ns must be in (0, 10^10]. */
 fp8_status_t fp8_debug_wait_probe(int *dev_status, uint64_t timeout_ns, fp8_stream_t stream);
+
+/* Checks of the GEMM kernels' timeout exit (no counterpart on the pages):
+ * fp8_gemm_blockscaled and fp8_gemm_mx, same arguments and rules, run on the
+ * single-CTA kernels only (no CTA-pair or split-K cluster kernel) with every
+ * bounded wait inside the kernel limited to wait_ns nanoseconds instead of 2 s.
+ * With a short limit a wait expires: the kernel writes FP8_ERR_TIMEOUT to
+ * *dev_status, waits (with its own fixed limit) for its copies and MMAs in
+ * flight, frees its tensor memory and returns; the output is then unspecified
+ * and the context stays usable. dev_status must be non-NULL; wait_ns in
+ * (0, 10^10]. */
+fp8_status_t fp8_debug_gemm_blockscaled_wait_limit(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,
+                                                   const void *b_dev, const float *b_scales_dev, fp8_gran_t b_gran,
+                                                   fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M,
+                                                   int64_t N, int64_t K, int *dev_status, uint64_t wait_ns,
+                                                   fp8_stream_t stream);
+fp8_status_t fp8_debug_gemm_mx_wait_limit(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                          const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt,
+                                          void *out_dev, int64_t M, int64_t N, int64_t K, int *dev_status,
+                                          uint64_t wait_ns, fp8_stream_t stream);
 
 /* Number of kernel launches the library has enqueued since it was loaded
  * (all entry points, all devices); a diagnostic counter. */

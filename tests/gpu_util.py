@@ -76,3 +76,28 @@ def within_tolerance(got: np.ndarray, ref: np.ndarray, bound: np.ndarray) -> Tol
     tol = Tolerance(int(err.size), int(bad.sum()), worst, int(needed.sum()), worst_plain)
     RECORDS.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], tol))
     return tol
+
+
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """A device buffer with GUARD_BYTES of a known byte on each side (a stand-in for
+    a memory checker: any store that strays past either end of the buffer changes a
+    guard byte). .t is the tensor view handed to the library (16-byte aligned)."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        elt = torch.empty((), dtype=dtype).element_size()
+        n = 1
+        for s in shape:
+            n *= s
+        self.nbytes = n * elt
+        self.raw = torch.full((GUARD_BYTES + self.nbytes + GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device=device)
+        self.t = self.raw[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(dtype).view(*shape)
+
+    def intact(self) -> bool:
+        torch.cuda.synchronize()
+        lo = self.raw[:GUARD_BYTES]
+        hi = self.raw[GUARD_BYTES + self.nbytes:]
+        return bool((lo == GUARD_BYTE).all()) and bool((hi == GUARD_BYTE).all())

@@ -77,6 +77,8 @@ def test_quantize_refusals(L):
     assert _q(L, cols=120, ldx=128, ldq=128) == fb.ERR_UNSUPPORTED_SHAPE  # % 16
     assert _q(L, gran=2, cols=144, ldx=144, ldq=144) == fb.ERR_UNSUPPORTED_SHAPE  # % 128
     assert _q(L, gran=4, cols=48, ldx=48, ldq=48) == fb.ERR_UNSUPPORTED_SHAPE  # % 32
+    assert _q(L, gran=3, rows=65535 * 128 + 1) == fb.ERR_UNSUPPORTED_SHAPE  # 128x128 row blocks > grid y limit
+    assert _q(L, gran=3, rows=65535 * 128, sc=None) == fb.ERR_INVALID_ARG  # the largest accepted row count
     assert _q(L, ldx=64) == fb.ERR_INVALID_ARG  # ld < cols
     assert _q(L, x=MIS) == fb.ERR_ALIGNMENT
     assert _q(L, q=MIS) == fb.ERR_ALIGNMENT
@@ -140,6 +142,18 @@ def test_gemm_refusals(L):
     assert L.fp8_debug_wait_probe(None, 1000, None) == fb.ERR_INVALID_ARG
     assert L.fp8_debug_wait_probe(A16, 0, None) == fb.ERR_INVALID_ARG
     assert L.fp8_debug_encode_f32(A16, 12, 0, A16b, None) == fb.ERR_INVALID_ARG
+    assert fb.launch_count() == n0
+
+
+def test_gemm_wait_limit_refusals(L):
+    n0 = fb.launch_count()
+    g = L.fp8_debug_gemm_blockscaled_wait_limit
+    assert g(A16, A16, 2, A16b, A16, 3, 0, 0, A16, 16, 16, 128, None, 1000, None) == fb.ERR_INVALID_ARG  # no status
+    assert g(A16, A16, 2, A16b, A16, 3, 0, 0, A16, 16, 16, 128, A16, 0, None) == fb.ERR_INVALID_ARG  # limit 0
+    assert g(A16, A16, 2, A16b, A16, 3, 0, 0, A16, 16, 16, 144, A16, 1000, None) == fb.ERR_UNSUPPORTED_SHAPE
+    m = L.fp8_debug_gemm_mx_wait_limit
+    assert m(A16, A16, A16b, A16, 0, 0, A16, 16, 16, 64, A16, 10 ** 10 + 1, None) == fb.ERR_INVALID_ARG
+    assert m(A16, A16, A16b, A16, 0, 0, A16, 16, 16, 48, A16, 1000, None) == fb.ERR_UNSUPPORTED_SHAPE
     assert fb.launch_count() == n0
 
 

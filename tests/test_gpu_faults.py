@@ -52,3 +52,82 @@ def test_bad_shapes_refused():
     with pytest.raises(fb.Fp8Error) as e:
         fb.gemm_blockscaled(a2, s, fb.TILE_1x128, b, s, fb.BLOCK_128x128)  # N % 16 != 0
     assert e.value.code == fb.ERR_UNSUPPORTED_SHAPE
+
+
+# ------------------------------------------------------------ GEMM timeout exit
+# The single-CTA GEMM kernels run with every bounded wait limited to 1 ns: the
+# first wait that is not already satisfied expires, the kernel records
+# FP8_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns.
+# A normal GEMM on the same context afterwards must still match the oracle.
+import ctypes  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+import oracle  # noqa: E402
+from fp8_block_scaled_04_gb300 import synth  # noqa: E402
+from gpu_util import out_f64, within_tolerance  # noqa: E402
+
+_P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+_S = lambda: ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)  # noqa: E731
+
+# (name, M, N, K, a_gran, b_gran): the fold kernel with 256- and 128-wide tiles,
+# the operand-swapped decode kernel (no split-K cluster on this path), the
+# epilogue-scaled tensor-memory kernel, and the MXFP8 block-scaled kernel
+_CASES = [("fold_wide", 2048, 4096, 1024, fb.TILE_1x128, fb.BLOCK_128x128),
+          ("fold_narrow", 256, 1024, 2048, fb.TILE_1x128, fb.BLOCK_128x128),
+          ("swap", 16, 2048, 2048, fb.TILE_1x128, fb.BLOCK_128x128),
+          ("epi", 512, 1024, 1024, fb.TOKEN, fb.TOKEN),
+          ("mx", 1024, 1024, 1024, fb.MX32, fb.MX32)]
+
+
+@pytest.mark.parametrize("name,M,N,K,ga,gb", _CASES, ids=[c[0] for c in _CASES])
+def test_gemm_timeout_exit_then_context_usable(name, M, N, K, ga, gb):
+    L = fb.lib()
+    x = synth.bf16_matrix(M, K, 1.0, 700 + M, 701, 0.01, 30.0)
+    w = synth.bf16_matrix(N, K, 0.02, 702 + N)
+    lay = fb.SF_TCGEN05 if ga == fb.MX32 else fb.SF_LINEAR
+    qa, sa = oracle.quantize(x, fb.E4M3, ga, lay)
+    qb, sb = oracle.quantize(w, fb.E4M3, gb, lay)
+    a, sad, b, sbd = (torch.from_numpy(t).cuda() for t in (qa, sa, qb, sb))
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes = []
+    for _ in range(5):
+        status.zero_()
+        if ga == fb.MX32:
+            rc = L.fp8_debug_gemm_mx_wait_limit(_P(a), _P(sad), _P(b), _P(sbd), 0, 0, _P(out), M, N, K, _P(status), 1,
+                                                _S())
+        else:
+            rc = L.fp8_debug_gemm_blockscaled_wait_limit(_P(a), _P(sad), ga, _P(b), _P(sbd), gb, 0, 0, _P(out), M, N,
+                                                         K, _P(status), 1, _S())
+        assert rc == fb.OK
+        torch.cuda.synchronize()
+        codes.append(int(status.item()))
+        if codes[-1] == fb.ERR_TIMEOUT:
+            break
+    assert set(codes) <= {fb.OK, fb.ERR_TIMEOUT} and codes[-1] == fb.ERR_TIMEOUT, codes
+    # the context still works: the same GEMM with the production limit matches the oracle
+    status.zero_()
+    out.zero_()
+    if ga == fb.MX32:
+        fb.gemm_mx(a, sad, b, sbd, out=out, status=status)
+    else:
+        fb.gemm_blockscaled(a, sad, ga, b, sbd, gb, out=out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fb.OK
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 64)), [M - 1]]))
+    kw = dict(a_sf=lay, b_sf=lay) if ga == fb.MX32 else {}
+    ref, bound = oracle.gemm(qa, sa, ga, qb, sb, gb, rows=rows, **kw)
+    tol = within_tolerance(out_f64(out)[rows], ref, bound)
+    assert tol.bad == 0, tol
+
+
+def test_default_status_word_reports_timeouts():
+    """The binding's per-device status word (used when a GEMM wrapper gets no status)
+    carries a timeout to check_status(), which raises and clears it."""
+    st = fb.default_status()
+    st.fill_(fb.ERR_TIMEOUT)  # what an expired wait leaves there
+    with pytest.raises(fb.Fp8Error) as e:
+        fb.check_status()
+    assert e.value.code == fb.ERR_TIMEOUT
+    fb.check_status()  # cleared
