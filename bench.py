@@ -33,6 +33,10 @@ M, N, K = 4096, 14336, 4096
 WORKLOAD = ("prefill FP8 linear: X bf16 4096x4096 -> E4M3 1x128 tile scales (dynamic), "
             "W E4M3 14336x4096 128x128 block scales (offline), Out bf16 4096x14336")
 NOMINAL_FP8_PFLOPS = 4.5
+# FP4 peak over FP8 peak: "Low precision: FP8, FP4, and microscaling" gives 4.5 and
+# 9 PFLOPS dense for FP8 and FP4 on B200 (ratio 2); the hardware table for GB300
+# lists 13.5 PF dense FP4, which the NVFP4 line reports beside it
+FP4_OVER_FP8 = 2.0
 
 
 def measured_peaks():
@@ -163,6 +167,76 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
     return world * units_per_rank / (slowest_ms * 1e-3)
 
 
+def rank_env():
+    """(world, rank, local_rank) from the launcher's environment (1, 0, 0 without one)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def gather_ranks(obj):
+    """Every rank's obj, in rank order (a one-element list with one process)."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [obj]
+    out = [None] * dist.get_world_size()
+    dist.all_gather_object(out, obj)
+    return out
+
+
+def free_port() -> int:
+    import socket
+
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def spawn_replicas(n: int, argv) -> int:
+    """Run this script as n ranks of one node (one process per GPU, replicas of the
+    step, no data-path collective) under torch.distributed.run, the way a multi-GPU
+    launch would; rank 0 prints the JSON line. Returns the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def run_stub(args):
+    """The rank plumbing of the GPU arm with a CPU stand-in for the step (a fixed
+    sleep that grows with the rank, so the ranks differ): gloo process group,
+    per-rank device choice, barrier-bracketed timing of exactly K steps after W
+    warm-up steps, the slowest rank's time and the whole-job rate. Prints the same
+    JSON keys, marked "stub"; it measures nothing about the kernels."""
+    import torch.distributed as dist
+
+    world, rank, local = rank_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    step_s = 0.002 * (1 + rank)
+    for _ in range(args.warmup):
+        time.sleep(step_s)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time.sleep(step_s)
+    if world > 1:
+        dist.barrier()
+    ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    slow = max_over_ranks(ms)
+    devices = gather_ranks("cpu:%d" % local)
+    per_rank_ms = gather_ranks(ms)
+    if rank == 0:
+        print(json.dumps({"metric": "stub steps/s", "value": whole_job_rate(1.0, world, slow), "unit": "steps/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": slow,
+                          "higher_is_better": True, "scaling": "weak", "stub": True, "devices": devices,
+                          "per_rank_ms": per_rank_ms}))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 # --------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import numpy as np
@@ -172,13 +246,12 @@ def run_gpu(args):
     from fp8_block_scaled_04_gb300 import binding as fb
     from fp8_block_scaled_04_gb300 import synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    devices = gather_ranks(str(dev))
     stream = torch.cuda.current_stream()
     peaks = measured_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # fp8 = 2 x bf16 (nominal 4.5 / 2.25 PF)
@@ -310,6 +383,8 @@ def run_gpu(args):
         extra = measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak)
 
     cpu = cpu_baseline_sample(x_host, w_host) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if extra and rank == 0 and world == 1 and not args.no_cpu:
+        cpu_baselines_other(extra, synth)
 
     if rank == 0:
         line = {
@@ -328,11 +403,18 @@ def run_gpu(args):
                          "peak_src": "%s bf16 burst x2 (fp8/bf16 nominal ratio)" % peaks["src"],
                          "frac_of_nominal_4.5PF": round(achieved / (NOMINAL_FP8_PFLOPS * 1000.0), 4),
                          "traffic": kernel_traffic("gemm_fold_kernel"),
-                         "algorithmic_bytes": 2 * M * K + N * K + 2 * M * N + 4 * (K // 128) * (M + (N // 128))},
+                         # the GEMM's compulsory bytes: fp8 X and W read once, bf16 Out written once, scales
+                         "algorithmic_bytes": M * K + N * K + 2 * M * N + 4 * (K // 128) * (M + (N // 128)),
+                         "algorithmic_flops": 2 * M * N * K,
+                         # the whole step adds the 1x128 quantize of X (bf16 read, codes and scales written)
+                         # and the GEMM's re-read of the codes (already counted above)
+                         "step_algorithmic_bytes": (2 * M * K + M * K + 4 * (K // 128) * M) + M * K + N * K
+                                                   + 2 * M * N + 4 * (K // 128) * (M + (N // 128))},
             "e2e": {"value": round(whole_job_rate(flops, world, e2e) / 1e12, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2, "ms_per_step": round(e2e, 4),
                     "pipelining": "3 streams (upload / compute / download), 2 buffers each, across steps"},
             "gpu_launches": int(launches),
+            "devices": devices,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
         }
@@ -366,8 +448,18 @@ def _time_kernel(fn, flush, stream, reps, launches=1):
     return statistics.median(a.elapsed_time(b) for a, b in ts)
 
 
+NOMINAL_HBM_GBS = 8000.0  # "~8 TB/s" HBM3e, the quantizers' stated target is 80 % of it
+
+
+def hbm_fracs(byts, t_ms, hbm_peak):
+    gbs = byts / (t_ms * 1e-3) / 1e9
+    return {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
+            "frac_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
 def measure_sweep(args, fb, synth, dev, stream, flush, hbm_peak):
-    """Quantizer sweep: 16384 x 8192, E4M3/E5M2 x {tensor (two-pass), token, 1x128, MX-32}."""
+    """Quantizer sweep: 16384 x 8192, E4M3/E5M2 x {tensor (two-pass), token, 1x128, MX-32}.
+    frac_hbm is against the measured copy bandwidth, frac_nominal_8TBs against 8 TB/s."""
     import numpy as np
     import torch
 
@@ -381,17 +473,109 @@ def measure_sweep(args, fb, synth, dev, stream, flush, hbm_peak):
     ws = torch.empty(256, dtype=torch.uint8, device=dev)
     sweep = {}
     for fname, fmt in (("e4m3", fb.E4M3), ("e5m2", fb.E5M2)):
-        for gname, gran in (("tensor", fb.TENSOR), ("token", fb.TOKEN), ("tile1x128", fb.TILE_1x128),
-                            ("mx32", fb.MX32)):
-            nb = fb.scales_bytes(R, C, gran)
+        for gname, gran, lay in (("tensor", fb.TENSOR, fb.SF_LINEAR), ("token", fb.TOKEN, fb.SF_LINEAR),
+                                 ("tile1x128", fb.TILE_1x128, fb.SF_LINEAR), ("mx32", fb.MX32, fb.SF_LINEAR),
+                                 ("mx32_tiled", fb.MX32, fb.SF_TCGEN05)):
+            nb = fb.scales_bytes(R, C, gran, lay)
             sc = torch.empty(max(nb, 4), dtype=torch.uint8, device=dev)
             scv = sc if gran == fb.MX32 else sc.view(torch.float32)
-            t = _time_kernel(lambda: fb.quantize(x, fmt, gran, q=q, scales=scv, workspace=ws), flush, stream, reps)
+            t = _time_kernel(lambda: fb.quantize(x, fmt, gran, lay, q=q, scales=scv, workspace=ws), flush, stream,
+                             reps)
             byts = R * C * 3 + nb + (R * C * 2 if gran == fb.TENSOR else 0)
-            gbs = byts / (t * 1e-3) / 1e9
-            sweep["%s_%s" % (fname, gname)] = {"ms": round(t, 5), "GB/s": round(gbs, 1),
-                                               "frac_hbm": round(gbs / hbm_peak, 4), "algorithmic_bytes": byts}
+            e = {"ms": round(t, 5), "algorithmic_bytes": byts}
+            e.update(hbm_fracs(byts, t, hbm_peak))
+            if gran == fb.TENSOR:
+                # the same time against one pass's bytes (read 2 B, write 1 B per element)
+                e["single_pass_equivalent"] = hbm_fracs(R * C * 3 + nb, t, hbm_peak)
+            sweep["%s_%s" % (fname, gname)] = e
     return sweep
+
+
+def measure_next_rows(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak):
+    """The rows built after the hot path, each against its roofline:
+    - the fold GEMM with 1x128 quantization fused into its epilogue, against the
+      GEMM's bf16 output followed by a separate 1x128 quantize of it ("Low
+      precision", practice 4: the separate pass costs two trips to HBM), on the
+      prefill shape 4096 x 14336 x 4096;
+    - per-tensor quantization with delayed scaling (one pass, scale from an amax
+      history) against current scaling (two passes) on the sweep tensor 16384 x 8192;
+    - per-channel quantization of a KV-cache-shaped tensor, 65536 tokens x 1024
+      channels (8 heads x 128 dims)."""
+    import numpy as np
+    import torch
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    reps = max(10, args.steps)
+    res = {}
+    # ---- fused quantize-in-epilogue (f1)
+    qx, sx = fb.quantize(to_dev(synth.prefill_x(M, K)), fb.E4M3, fb.TILE_1x128)
+    qw, sw = fb.quantize(to_dev(synth.prefill_w(N, K)), fb.E4M3, fb.BLOCK_128x128)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    qo = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    so = torch.empty((N // 128) * M, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    t_fused = _time_kernel(lambda: fb.gemm_blockscaled_quantized_out(qx, sx, qw, sw, q_out=qo, q_scales=so, status=st),
+                           flush, stream, reps)
+
+    def unfused():
+        fb.gemm_blockscaled(qx, sx, fb.TILE_1x128, qw, sw, fb.BLOCK_128x128, out=out, status=st)
+        fb.quantize(out, fb.E4M3, fb.TILE_1x128, q=qo, scales=so)
+
+    t_unfused = _time_kernel(unfused, flush, stream, reps, launches=2)
+    flops = 2.0 * M * N * K
+    gemm_in = M * K + N * K + 4 * (K // 128) * (M + N // 128)
+    fused_bytes = gemm_in + M * N + 4 * (N // 128) * M
+    unfused_bytes = gemm_in + 2 * M * N + (2 * M * N + M * N + 4 * (N // 128) * M)
+    res["fused_quantized_out_prefill"] = {
+        "fused": {"ms": round(t_fused, 5), "TFLOP/s": round(flops / (t_fused * 1e-3) / 1e12, 1),
+                  "frac_fp8_peak": round(flops / (t_fused * 1e-3) / 1e12 / fp8_peak, 4), "algorithmic_bytes": fused_bytes},
+        "gemm_then_quantize": {"ms": round(t_unfused, 5), "TFLOP/s": round(flops / (t_unfused * 1e-3) / 1e12, 1),
+                               "algorithmic_bytes": unfused_bytes},
+        "hbm_bytes_saved": unfused_bytes - fused_bytes, "speedup": round(t_unfused / t_fused, 4),
+        "output": "E4M3 codes + 1x128 scales of the bf16-rounded GEMM output (the next layer's activation)"}
+    del qx, sx, qw, sw, out, qo, so
+    # ---- delayed vs current per-tensor scaling (f3)
+    R, C = 16384, 8192
+    x = to_dev(synth.sweep_x(R, C))
+    q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    scale = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    hist = torch.zeros(16, dtype=torch.float32, device=dev)
+    fb.quantize_delayed(x, fb.E4M3, hist, 0)  # a history with this tensor's amax in it
+    slot = [0]
+
+    def delayed():
+        slot[0] = (slot[0] + 1) % 16
+        fb.quantize_delayed(x, fb.E4M3, hist, slot[0], q=q, scale=scale)
+
+    t_del = _time_kernel(delayed, flush, stream, reps, launches=2)
+    t_cur = _time_kernel(lambda: fb.quantize(x, fb.E4M3, fb.TENSOR, q=q, scales=scale, workspace=ws), flush, stream,
+                         reps, launches=2)
+    one_pass = R * C * 3 + 4
+    res["delayed_vs_current_per_tensor_16384x8192"] = {
+        "delayed_one_pass": dict({"ms": round(t_del, 5), "algorithmic_bytes": one_pass}, **hbm_fracs(one_pass, t_del, hbm_peak)),
+        "current_two_pass": dict({"ms": round(t_cur, 5), "algorithmic_bytes": R * C * 5 + 4},
+                                 **hbm_fracs(R * C * 5 + 4, t_cur, hbm_peak)),
+        "speedup": round(t_cur / t_del, 4), "history_len": 16}
+    del x, q
+    # ---- per-channel KV-cache quantizer (f4)
+    T, Ch = 65536, 1024
+    kv = to_dev(synth.bf16_matrix(T, Ch, 1.0, 41, 42, 0.01, 20.0))
+    qk = torch.empty((T, Ch), dtype=torch.uint8, device=dev)
+    sk = torch.empty(Ch, dtype=torch.float32, device=dev)
+    wk = torch.empty(fb.workspace_bytes(T, Ch, fb.CHANNEL), dtype=torch.uint8, device=dev)
+    res_kv = {}
+    for fname, fmt in (("e4m3", fb.E4M3), ("e5m2", fb.E5M2)):
+        t_kv = _time_kernel(lambda: fb.quantize(kv, fmt, fb.CHANNEL, q=qk, scales=sk, workspace=wk), flush, stream,
+                            reps, launches=3)
+        byts = T * Ch * 5 + 4 * Ch  # column maxima pass (2 B) + encode pass (2 B read, 1 B written)
+        res_kv[fname] = dict({"ms": round(t_kv, 5), "algorithmic_bytes": byts,
+                              "single_pass_equivalent": hbm_fracs(T * Ch * 3 + 4 * Ch, t_kv, hbm_peak)},
+                             **hbm_fracs(byts, t_kv, hbm_peak))
+    res["kv_cache_per_channel_65536x1024"] = res_kv
+    return res
 
 
 def measure_decode(args, fb, synth, dev, stream, flush, hbm_peak):
@@ -490,7 +674,8 @@ def measure_nvfp4(args, fb, synth, dev, stream, flush, hbm_peak, fp4_peak):
     t = _time_kernel(lambda: fb.gemm_nvfp4(qa, sfa, ta, qb, sfb, tb, out=o), flush, stream, reps)
     tf = 2.0 * S ** 3 / (t * 1e-3) / 1e12
     res["nvfp4_gemm_8192"] = {"ms": round(t, 5), "TFLOP/s": round(tf, 1), "frac_fp4_peak": round(tf / fp4_peak, 4),
-                              "fp4_peak_src": "measured bf16 burst x 6 (fp4/bf16 nominal ratio 13.5/2.25)",
+                              "fp4_peak": round(fp4_peak, 1),
+                              "fp4_peak_src": "measured bf16 burst x 2 (fp8) x 2 (fp4 = 2 x fp8, the pages' 9 vs 4.5 PF)",
                               "frac_nominal_13.5PF": round(tf / 13500.0, 4)}
     return res
 
@@ -512,7 +697,10 @@ def run_workload(args):
     elif args.workload == "decode":
         res = measure_decode(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"])
     elif args.workload == "nvfp4":
-        res = measure_nvfp4(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"], 6.0 * peaks["bf16_tflops"])
+        res = measure_nvfp4(args, fb, synth, dev, stream, flush, peaks["hbm_gbs"],
+                            FP4_OVER_FP8 * 2.0 * peaks["bf16_tflops"])
+    elif args.workload == "next":
+        res = measure_next_rows(args, fb, synth, dev, stream, flush, 2.0 * peaks["bf16_tflops"], peaks["hbm_gbs"])
     else:
         res = measure_mx(args, fb, synth, dev, stream, flush, 2.0 * peaks["bf16_tflops"])
     print(json.dumps({"workload": args.workload, "peaks": peaks["src"], "results": res}))
@@ -523,11 +711,63 @@ def measure_other_workloads(args, fb, synth, dev, stream, flush, fp8_peak, hbm_p
     res = {"quantize_sweep_16384x8192": measure_sweep(args, fb, synth, dev, stream, flush, hbm_peak)}
     res.update(measure_decode(args, fb, synth, dev, stream, flush, hbm_peak))
     res.update(measure_mx(args, fb, synth, dev, stream, flush, fp8_peak))
-    res.update(measure_nvfp4(args, fb, synth, dev, stream, flush, hbm_peak, 3.0 * fp8_peak))
+    res.update(measure_nvfp4(args, fb, synth, dev, stream, flush, hbm_peak, FP4_OVER_FP8 * fp8_peak))
+    res.update(measure_next_rows(args, fb, synth, dev, stream, flush, fp8_peak, hbm_peak))
     return res
 
 
 # --------------------------------------------------------------------- CPU oracle
+def cpu_baselines_other(extra, synth, rows_sweep: int = 512, rows_mx: int = 16):
+    """The oracle, as it stands, on bounded samples of the other workloads (the first
+    rows of each input; the generator is counter-based, so those rows are the full
+    input's): the quantizer sweep on rows_sweep of its 16384 rows, both decode GEMMs in
+    full, the MXFP8 GEMM on rows_mx of its 8192 rows. Attached to each workload's entry
+    as "cpu_baseline"; the units match the GPU figure beside it."""
+    import oracle
+
+    threads = oracle.default_threads()
+    C = 8192
+    xs = synth.sweep_x(rows_sweep, C)
+    sw = extra.get("quantize_sweep_16384x8192", {})
+    for fname, fmt in (("e4m3", oracle.E4M3), ("e5m2", oracle.E5M2)):
+        for gname, gran, lay in (("tensor", oracle.TENSOR, 0), ("token", oracle.TOKEN, 0),
+                                 ("tile1x128", oracle.TILE_1x128, 0), ("mx32", oracle.MX32, 0),
+                                 ("mx32_tiled", oracle.MX32, 1)):
+            key = "%s_%s" % (fname, gname)
+            if key not in sw:
+                continue
+            t0 = time.perf_counter()
+            oracle.quantize(xs, fmt, gran, lay)
+            dt = time.perf_counter() - t0
+            byts = sw[key]["algorithmic_bytes"] * rows_sweep / 16384.0
+            sw[key]["cpu_baseline"] = {"value": round(byts / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+                                       "kind": "oracle", "sample": "first %d of 16384 rows" % rows_sweep}
+    Nd, Kd = 18432, 7168
+    wq, wsc = oracle.quantize(synth.decode_w(Nd, Kd), oracle.E4M3, oracle.BLOCK_128x128)
+    for m in (16, 64):
+        key = "decode_gemm_m%d" % m
+        if key not in extra:
+            continue
+        xq, xsc = oracle.quantize(synth.decode_x(m, Kd), oracle.E4M3, oracle.TILE_1x128)
+        t0 = time.perf_counter()
+        oracle.gemm(xq, xsc, oracle.TILE_1x128, wq, wsc, oracle.BLOCK_128x128)
+        dt = time.perf_counter() - t0
+        extra[key]["cpu_baseline"] = {"value": round(extra[key]["algorithmic_bytes"] / dt / 1e9, 3), "unit": "GB/s",
+                                      "TFLOP/s": round(2.0 * m * Nd * Kd / dt / 1e12, 5), "cores": threads,
+                                      "kind": "oracle", "sample": "the whole GEMM (fp64 sums), W quantized beforehand"}
+    del wq, wsc
+    if "mx_gemm_8192" in extra:
+        S = 8192
+        xq, xsf = oracle.quantize(synth.mx_x(rows_mx, S), oracle.E4M3, oracle.MX32, 1)
+        wq, wsf = oracle.quantize(synth.mx_w(S, S), oracle.E4M3, oracle.MX32, 1)
+        t0 = time.perf_counter()
+        oracle.gemm(xq, xsf, oracle.MX32, wq, wsf, oracle.MX32, a_sf=1, b_sf=1)
+        dt = time.perf_counter() - t0
+        extra["mx_gemm_8192"]["cpu_baseline"] = {"value": round(2.0 * rows_mx * S * S / dt / 1e12, 5),
+                                                 "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                                 "sample": "first %d of 8192 rows of X, all of W, fp64 sums" % rows_mx}
+
+
 def cpu_baseline_sample(x_host, w_host, target_s: float = 10.0):
     """The oracle as it stands, on a bounded sample of the headline workload:
     quantize the first R rows of X (1x128), quantize W (128x128), and the fp64
@@ -599,13 +839,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--headline-only", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "sweep", "decode", "mx", "nvfp4"],
+    ap.add_argument("--workload", default="all", choices=["all", "sweep", "decode", "mx", "nvfp4", "next"],
                     help="all: the headline step plus the other workloads; otherwise that workload alone")
-    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baselines")
+    ap.add_argument("--stub-step", action="store_true",
+                    help="check of the rank plumbing on CPU: a sleep stands in for the step (measures nothing)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_replicas(args.gpus, sys.argv[1:]))
+    if args.stub_step:
+        run_stub(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.workload != "all":
         run_workload(args)

@@ -51,3 +51,28 @@ def test_single_process_is_identity():
 
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.whole_job_rate(2.0, 1, 1000.0) == 2.0
+
+
+def test_bench_spawns_replica_ranks_itself():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself (through
+    torch.distributed.run); with the CPU stand-in step they use gloo, each picks the
+    device of its local rank, and rank 0 reports the slowest rank's time and the
+    work of both."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+                                                            "MASTER_PORT")}
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--stub-step", "--steps", "5",
+                        "--warmup", "3"], capture_output=True, text=True, env=env, timeout=300, cwd=root)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, p.stdout  # rank 0 alone prints
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["stub"] is True
+    assert rec["devices"] == ["cpu:0", "cpu:1"]
+    assert rec["ms_per_step"] == pytest.approx(max(rec["per_rank_ms"]))
+    assert rec["per_rank_ms"][1] > rec["per_rank_ms"][0]  # rank 1's step is the slower one
+    assert rec["value"] == pytest.approx(2 * 1.0 / (rec["ms_per_step"] * 1e-3))
