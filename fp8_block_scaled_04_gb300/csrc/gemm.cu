@@ -838,11 +838,17 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
     tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
+  // the first stages' W boxes of this CTA's first tile go to L2 while the
+  // previous kernel finishes (a prefetch reads nothing into this kernel)
+  if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < ntiles) {
+    const int wt = static_cast<int>(blockIdx.x) / num_x;
+    for (int kb = 0; kb < STAGES && kb < KB; ++kb) tma_prefetch_l2_2d(&tmW, kb * BK, wt * BM);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   // dependent launch: the setup above overlaps the previous kernel's tail;
-  // nothing it writes (X, the scales, Out) is touched before this wait
+  // nothing it writes (X, the scales, Out) is read into this kernel before this wait
   grid_dependents_launch();
   grid_dependency_wait();
   const uint32_t tmem = ctl.tmem_base;
@@ -1046,6 +1052,10 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
   if (warp == 1) {
     tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0 && first_tile < ntiles) {  // as in the unsplit kernel
+    const int wt = first_tile / num_x;
+    for (int kb = kb_lo; kb < kb_hi && kb < kb_lo + STAGES; ++kb) tma_prefetch_l2_2d(&tmW, kb * BK, wt * BM);
   }
   tc_fence_before();
   __syncthreads();

@@ -103,6 +103,15 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
+// Prefetch a 2-D box into L2 (no shared-memory destination, no completion to
+// wait for). L2 is where the GPU's global memory is kept coherent, so a
+// prefetch is harmless even while another kernel may still be writing the box.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
   asm volatile(

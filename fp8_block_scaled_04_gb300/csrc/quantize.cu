@@ -377,36 +377,77 @@ __global__ void __launch_bounds__(kThreads) quant_block_kernel(const uint16_t *_
 }
 
 // ------------------------------------------------------------ per-channel
-// One scale per column (two passes, like per-tensor). A CTA owns a strip of
-// kChanCols columns (256 threads x 8 columns) and a chunk of rows; each row of
-// the strip is one contiguous 4 KB segment, read with 16-byte loads, four rows
-// in flight per thread.
-constexpr int kChanCols = kThreads * 8;
+// One scale per column (two passes, like per-tensor). A CTA owns a strip of at
+// most 256 16-byte column vectors (2048 columns) and a chunk of rows. When the
+// strip is narrower than 256 vectors the CTA's threads form several row slabs
+// (slab = thread / strip width), so every thread loads: a thread keeps one
+// vector (8 columns) and walks the rows r0 + slab, r0 + slab + slabs, ...,
+// eight rows in flight. Pass 1 keeps the column maxima in registers, combines
+// the slabs in shared memory and issues one atomicMax per column per CTA. Pass
+// 2 walks each chunk's rows in reverse, so the rows pass 1 read last (still in
+// L2) come first.
+constexpr int kChanRows = 8;  // rows in flight per thread
+#ifndef FP8BS_CHAN_CTAS_PER_SM
+#define FP8BS_CHAN_CTAS_PER_SM 2  // row chunks: about this many CTAs per SM
+#endif
+
+struct ChanGeom {
+  int64_t strip_vec;  // vectors per strip (<= kThreads)
+  int slabs;          // row slabs per CTA
+};
+
+__host__ __device__ inline ChanGeom chan_geom(int64_t cols) {
+  const int64_t vec = cols / 8;
+  ChanGeom g;
+  g.strip_vec = vec < kThreads ? vec : kThreads;
+  g.slabs = static_cast<int>(kThreads / g.strip_vec);
+  return g;
+}
 
 __global__ void __launch_bounds__(kThreads) channel_amax_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                 int64_t cols, int64_t ldx, int64_t rows_per_cta,
                                                                 uint32_t *__restrict__ col_amax) {
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChanCols + threadIdx.x * 8;
+  const ChanGeom g = chan_geom(cols);
+  const int slab = static_cast<int>(threadIdx.x / g.strip_vec);
+  const int64_t v = static_cast<int64_t>(blockIdx.x) * g.strip_vec + threadIdx.x % g.strip_vec;
+  const bool active = slab < g.slabs && v < cols / 8;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
   const int64_t r1 = min(rows, r0 + rows_per_cta);
-  if (c0 >= cols) return;
   uint32_t m2[4] = {0u, 0u, 0u, 0u};  // packed 16-bit magnitude maxima of column pairs
-  for (int64_t r = r0; r < r1; r += 4) {
-    uint4 v[4];
+  if (active) {
+    for (int64_t r = r0 + slab; r < r1; r += static_cast<int64_t>(kChanRows) * g.slabs) {
+      uint4 vv[kChanRows];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = r + i < r1 ? ld_stream_v4(x + (r + i) * ldx + c0) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kChanRows; ++i) {
+        const int64_t ri = r + static_cast<int64_t>(i) * g.slabs;
+        vv[i] = ri < r1 ? ld_stream_v4(x + ri * ldx + v * 8) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      m2[0] = __vmaxu2(m2[0], v[i].x & 0x7fff7fffu);
-      m2[1] = __vmaxu2(m2[1], v[i].y & 0x7fff7fffu);
-      m2[2] = __vmaxu2(m2[2], v[i].z & 0x7fff7fffu);
-      m2[3] = __vmaxu2(m2[3], v[i].w & 0x7fff7fffu);
+      for (int i = 0; i < kChanRows; ++i) {
+        m2[0] = __vmaxu2(m2[0], vv[i].x & 0x7fff7fffu);
+        m2[1] = __vmaxu2(m2[1], vv[i].y & 0x7fff7fffu);
+        m2[2] = __vmaxu2(m2[2], vv[i].z & 0x7fff7fffu);
+        m2[3] = __vmaxu2(m2[3], vv[i].w & 0x7fff7fffu);
+      }
     }
   }
+  // combine the slabs: slab 0 of each vector takes the maximum over the others
+  __shared__ uint4 part[kThreads];
+  part[threadIdx.x] = make_uint4(m2[0], m2[1], m2[2], m2[3]);
+  __syncthreads();
+  if (active && slab == 0) {
+    for (int s = 1; s < g.slabs; ++s) {
+      const uint4 o = part[threadIdx.x + s * g.strip_vec];
+      m2[0] = __vmaxu2(m2[0], o.x);
+      m2[1] = __vmaxu2(m2[1], o.y);
+      m2[2] = __vmaxu2(m2[2], o.z);
+      m2[3] = __vmaxu2(m2[3], o.w);
+    }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    atomicMax(col_amax + c0 + 2 * j, (m2[j] & 0xffffu) << 16);
-    atomicMax(col_amax + c0 + 2 * j + 1, m2[j] & 0xffff0000u);
+    for (int j = 0; j < 4; ++j) {
+      atomicMax(col_amax + v * 8 + 2 * j, (m2[j] & 0xffffu) << 16);
+      atomicMax(col_amax + v * 8 + 2 * j + 1, m2[j] & 0xffff0000u);
+    }
   }
 }
 
@@ -416,29 +457,38 @@ __global__ void __launch_bounds__(kThreads) channel_quant_kernel(const uint16_t 
                                                                  const uint32_t *__restrict__ col_amax,
                                                                  uint8_t *__restrict__ q, int64_t ldq,
                                                                  float *__restrict__ scales) {
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChanCols + threadIdx.x * 8;
+  const ChanGeom g = chan_geom(cols);
+  const int slab = static_cast<int>(threadIdx.x / g.strip_vec);
+  const int64_t v = static_cast<int64_t>(blockIdx.x) * g.strip_vec + threadIdx.x % g.strip_vec;
+  if (slab >= g.slabs || v >= cols / 8) return;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
   const int64_t r1 = min(rows, r0 + rows_per_cta);
-  if (c0 >= cols) return;
   float s_inv[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     float s;
-    scale_pair(__uint_as_float(col_amax[c0 + j]), vmax_of(FMT), s, s_inv[j]);
-    if (blockIdx.y == 0) scales[c0 + j] = s;
+    scale_pair(__uint_as_float(col_amax[v * 8 + j]), vmax_of(FMT), s, s_inv[j]);
+    if (blockIdx.y == 0 && slab == 0) scales[v * 8 + j] = s;
   }
-  for (int64_t r = r0; r < r1; r += 4) {
-    uint4 v[4];
+  // this thread's rows r0 + slab + slabs * k, k = 0 .. n-1, taken from the last
+  if (r0 + slab >= r1) return;
+  const int64_t n = (r1 - 1 - (r0 + slab)) / g.slabs + 1;
+  for (int64_t k1 = n; k1 > 0; k1 -= kChanRows) {
+    uint4 vv[kChanRows];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = r + i < r1 ? ld_stream_v4(x + (r + i) * ldx + c0) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < kChanRows; ++i) {
+      const int64_t k = k1 - 1 - i;
+      vv[i] = k >= 0 ? ld_stream_v4(x + (r0 + slab + k * g.slabs) * ldx + v * 8) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (r + i >= r1) continue;
+    for (int i = 0; i < kChanRows; ++i) {
+      const int64_t k = k1 - 1 - i;
+      if (k < 0) continue;
       float f[8];
-      bf16x8_to_f32(v[i], f);
+      bf16x8_to_f32(vv[i], f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], s_inv[j]);
-      *reinterpret_cast<uint2 *>(q + (r + i) * ldq + c0) = encode8<FMT>(f, 1.0f);
+      *reinterpret_cast<uint2 *>(q + (r0 + slab + k * g.slabs) * ldq + v * 8) = encode8<FMT>(f, 1.0f);
     }
   }
 }
@@ -625,13 +675,14 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
       uint32_t *col_amax = static_cast<uint32_t *>(workspace);
       if (cudaMemsetAsync(col_amax, 0, static_cast<size_t>(cols) * sizeof(uint32_t), stream) != cudaSuccess)
         return FP8_ERR_CUDA;
-      const int64_t strips = (cols + kChanCols - 1) / kChanCols;
-      int64_t chunks = (static_cast<int64_t>(device_sm_count()) * 8 + strips - 1) / strips;
-      const int64_t max_chunks = (rows + 3) / 4;
+      // strips of <= 256 vectors; row chunks so that about FP8BS_CHAN_CTAS_PER_SM CTAs run per SM
+      const ChanGeom cg = chan_geom(cols);
+      const int64_t strips = (cols / 8 + cg.strip_vec - 1) / cg.strip_vec;
+      int64_t chunks = (static_cast<int64_t>(device_sm_count()) * FP8BS_CHAN_CTAS_PER_SM + strips - 1) / strips;
+      const int64_t max_chunks = (rows + cg.slabs - 1) / cg.slabs;
       if (chunks > max_chunks) chunks = max_chunks;
       if (chunks < 1) chunks = 1;
-      int64_t rpc = (rows + chunks - 1) / chunks;
-      rpc = (rpc + 3) / 4 * 4;
+      const int64_t rpc = (rows + chunks - 1) / chunks;
       chunks = (rows + rpc - 1) / rpc;
       dim3 g(static_cast<unsigned>(strips), static_cast<unsigned>(chunks));
       channel_amax_kernel<<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax);
