@@ -100,7 +100,10 @@ __device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32],
 #define NVF4_COPIERS 2  // scale-copier warps of the NVFP4 GEMM (12 atom copies per k-block)
 #endif
 #ifndef SF_COPIER
-#define SF_COPIER 1  // block-scaled GEMMs: a separate warp copies scale atoms to tensor memory
+#define SF_COPIER 1  // block-scaled GEMMs: separate warps may copy scale atoms to tensor memory
+#endif
+#ifndef MX8_COPIER
+#define MX8_COPIER 0  // MXFP8: 0 = the MMA thread copies a stage's three atoms itself (+2.4 %), 1 = a copier warp
 #endif
 #ifndef FOLD_USE_PAIRS
 #define FOLD_USE_PAIRS 0  // 1: block-scaled GEMMs with M > 128 run on CTA pairs (measured slower)
@@ -1239,18 +1242,20 @@ struct AccCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
   static constexpr int CONSUMER_WARPS = 4 * (BN / 128);
-  // warp 0 producer, warp 1 MMA issuer, (block-scaled kinds) warp 2 copies the
-  // stage's scale atoms into tensor memory, then the epilogue warps
-  static constexpr bool COPIER = MX && SF_COPIER;
+  // warp 0 producer, warp 1 MMA issuer, (NVFP4) warps 2 and 3 copy the stage's
+  // scale atoms into tensor memory, then the epilogue warps. MXFP8 has three
+  // atoms per stage: the MMA thread copies them right before its MMAs (a copier
+  // warp and its ready barrier put ~400 cycles of hand-off on the stage ring,
+  // which is latency-bound; 2.4 % slower, same-process A/B).
+  static constexpr bool COPIER = MX && SF_COPIER && (KIND == KIND_NVF4 || MX8_COPIER);
   // copier warps: the stage's atoms are split round-robin between them
   static constexpr int COPIERS = !COPIER ? 0 : (KIND == KIND_NVF4 ? NVF4_COPIERS : 1);
   static constexpr int FIRST_CONSUMER_WARP = 2 + COPIERS;
   // NVFP4 (12 atom copies per stage): the atoms travel on their own barrier
   // (sf_full) so the copiers start before the operands land, and the MMA
-  // thread waits for both (measured +4 %). MXFP8 (3 copies): the copier waits
-  // for the whole stage and sf_ready implies full (the MMA thread's second
-  // wait cost it 3 %; a copier that waits for its own copies before
-  // signalling cost 17 %).
+  // thread waits for both (measured +4 %). With an MXFP8 copier warp
+  // (MX8_COPIER) the copier waits for the whole stage and sf_ready implies
+  // full.
   static constexpr bool SF_SPLIT = COPIER && KIND == KIND_NVF4;
   static constexpr int THREADS = 32 * FIRST_CONSUMER_WARP + 32 * CONSUMER_WARPS;
   static constexpr int SF_COLS = 4 * ATOMS * (1 + BN / 128);  // tensor-memory columns per stage
@@ -1585,7 +1590,10 @@ bool ensure_smem(KernelT kernel, int bytes) {
 }
 
 // X rows a raster group may hold: well inside one die's half of the L2.
-constexpr int64_t kRasterGroupBytes = int64_t{32} << 20;
+#ifndef FP8BS_RASTER_MB
+#define FP8BS_RASTER_MB 32
+#endif
+constexpr int64_t kRasterGroupBytes = int64_t{FP8BS_RASTER_MB} << 20;
 
 int raster_group(int64_t M, int64_t K) {
   const int64_t num_m = (M + BM - 1) / BM;

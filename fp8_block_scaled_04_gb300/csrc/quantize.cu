@@ -386,7 +386,10 @@ __global__ void __launch_bounds__(kThreads) quant_block_kernel(const uint16_t *_
 // the slabs in shared memory and issues one atomicMax per column per CTA. Pass
 // 2 walks each chunk's rows in reverse, so the rows pass 1 read last (still in
 // L2) come first.
-constexpr int kChanRows = 8;  // rows in flight per thread
+#ifndef FP8BS_CHAN_ROWS
+#define FP8BS_CHAN_ROWS 8
+#endif
+constexpr int kChanRows = FP8BS_CHAN_ROWS;  // rows in flight per thread
 #ifndef FP8BS_CHAN_CTAS_PER_SM
 #define FP8BS_CHAN_CTAS_PER_SM 2  // row chunks: about this many CTAs per SM
 #endif

@@ -249,3 +249,4 @@ def test_dependent_launches_keep_stream_order(M):
         ref, bound = oracle.gemm(hq_o, hs_o, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
         tol = within_tolerance(out_f64(o), ref, bound)
         assert tol.bad == 0, tol
+
