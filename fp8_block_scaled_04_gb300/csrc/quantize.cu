@@ -395,22 +395,30 @@ constexpr int kChanRows = FP8BS_CHAN_ROWS;  // rows in flight per thread
 #endif
 
 struct ChanGeom {
-  int64_t strip_vec;  // vectors per strip (<= kThreads)
+  int64_t strip_vec;  // vectors per strip (<= 256)
   int slabs;          // row slabs per CTA
 };
 
-__host__ __device__ inline ChanGeom chan_geom(int64_t cols) {
+// Strips of at most 256 vectors; a CTA of `threads` threads forms
+// threads / strip_vec row slabs.
+__host__ __device__ inline ChanGeom chan_geom(int64_t cols, int threads = kThreads) {
   const int64_t vec = cols / 8;
   ChanGeom g;
   g.strip_vec = vec < kThreads ? vec : kThreads;
-  g.slabs = static_cast<int>(kThreads / g.strip_vec);
+  g.slabs = static_cast<int>(threads / g.strip_vec);
   return g;
 }
 
-__global__ void __launch_bounds__(kThreads) channel_amax_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                                int64_t cols, int64_t ldx, int64_t rows_per_cta,
-                                                                uint32_t *__restrict__ col_amax) {
-  const ChanGeom g = chan_geom(cols);
+// The amax pass runs 1024-thread CTAs (four times the slabs of the encode
+// pass's 256-thread CTAs, the same number of CTAs and atomics): it reads
+// every byte from HBM and needs the warps to keep enough loads in flight.
+constexpr int kChanAmaxThreads = 1024;
+
+__global__ void __launch_bounds__(kChanAmaxThreads) channel_amax_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                        int64_t cols, int64_t ldx,
+                                                                        int64_t rows_per_cta,
+                                                                        uint32_t *__restrict__ col_amax) {
+  const ChanGeom g = chan_geom(cols, kChanAmaxThreads);
   const int slab = static_cast<int>(threadIdx.x / g.strip_vec);
   const int64_t v = static_cast<int64_t>(blockIdx.x) * g.strip_vec + threadIdx.x % g.strip_vec;
   const bool active = slab < g.slabs && v < cols / 8;
@@ -420,10 +428,12 @@ __global__ void __launch_bounds__(kThreads) channel_amax_kernel(const uint16_t *
   if (active) {
     for (int64_t r = r0 + slab; r < r1; r += static_cast<int64_t>(kChanRows) * g.slabs) {
       uint4 vv[kChanRows];
+      // rows past the chunk re-read its last row (a maximum does not change), so
+      // the eight loads carry no predicate and issue back to back
 #pragma unroll
       for (int i = 0; i < kChanRows; ++i) {
-        const int64_t ri = r + static_cast<int64_t>(i) * g.slabs;
-        vv[i] = ri < r1 ? ld_stream_v4(x + ri * ldx + v * 8) : make_uint4(0, 0, 0, 0);
+        const int64_t ri = min(r + static_cast<int64_t>(i) * g.slabs, r1 - 1);
+        vv[i] = ld_stream_v4(x + ri * ldx + v * 8);
       }
 #pragma unroll
       for (int i = 0; i < kChanRows; ++i) {
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) channel_amax_kernel(const uint16_t *
     }
   }
   // combine the slabs: slab 0 of each vector takes the maximum over the others
-  __shared__ uint4 part[kThreads];
+  __shared__ uint4 part[kChanAmaxThreads];
   part[threadIdx.x] = make_uint4(m2[0], m2[1], m2[2], m2[3]);
   __syncthreads();
   if (active && slab == 0) {
@@ -688,7 +698,7 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
       const int64_t rpc = (rows + chunks - 1) / chunks;
       chunks = (rows + rpc - 1) / rpc;
       dim3 g(static_cast<unsigned>(strips), static_cast<unsigned>(chunks));
-      channel_amax_kernel<<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax);
+      channel_amax_kernel<<<g, kChanAmaxThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax);
       if (e4)
         channel_quant_kernel<FP8_E4M3><<<g, kThreads, 0, stream>>>(x, rows, cols, ld_x, rpc, col_amax, q, ld_q,
                                                                    static_cast<float *>(scales));
