@@ -28,59 +28,71 @@ class Fp8Error(RuntimeError):
         super().__init__("%s failed: %s" % (what, status_string(code)))
 
 
+CHECK_LIB_PATH = os.path.join(HERE, "libfp8bs_check.so")
+
+
 def lib():
     """Load libfp8bs.so (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libfp8bs.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        i64, u64, i32, vp, sz = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
-        L.fp8_status_string.restype = ctypes.c_char_p
-        L.fp8_status_string.argtypes = [i32]
-        L.fp8_scales_bytes.restype = sz
-        L.fp8_scales_bytes.argtypes = [i64, i64, i32, i32]
-        L.fp8_quantize_workspace_bytes.restype = sz
-        L.fp8_quantize_workspace_bytes.argtypes = [i64, i64, i32]
-        L.fp8_quantize.restype = i32
-        L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, sz, vp]
-        L.fp8_quantize_tensor_noalloc.restype = i32
-        L.fp8_quantize_tensor_noalloc.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, vp]
-        L.fp8_quantize_delayed.restype = i32
-        L.fp8_quantize_delayed.argtypes = [vp, i64, i64, i64, i32, vp, i32, i32, i32, vp, i64, vp, vp]
-        L.fp8_dequantize.restype = i32
-        L.fp8_dequantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp]
-        L.fp8_gemm_blockscaled.restype = i32
-        L.fp8_gemm_blockscaled.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp, vp]
-        L.fp8_gemm_blockscaled_quantized_out.restype = i32
-        L.fp8_gemm_blockscaled_quantized_out.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp]
-        L.fp8_gemm_mx.restype = i32
-        L.fp8_gemm_mx.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
-        L.fp8_nvfp4_scales_bytes.restype = sz
-        L.fp8_nvfp4_scales_bytes.argtypes = [i64, i64, i32]
-        L.fp8_quantize_nvfp4.restype = i32
-        L.fp8_quantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, vp, sz, vp]
-        L.fp8_dequantize_nvfp4.restype = i32
-        L.fp8_dequantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp]
-        L.fp8_gemm_nvfp4.restype = i32
-        L.fp8_gemm_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
-        L.fp8_debug_gemm_blockscaled_pairs.restype = i32
-        L.fp8_debug_gemm_blockscaled_pairs.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
-        L.fp8_debug_encode_e2m1_f32.restype = i32
-        L.fp8_debug_encode_e2m1_f32.argtypes = [vp, i64, vp, vp]
-        L.fp8_debug_encode_f32.restype = i32
-        L.fp8_debug_encode_f32.argtypes = [vp, i64, i32, vp, vp]
-        L.fp8_debug_gemm_blockscaled_wait_limit.restype = i32
-        L.fp8_debug_gemm_blockscaled_wait_limit.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp,
-                                                             u64, vp]
-        L.fp8_debug_gemm_mx_wait_limit.restype = i32
-        L.fp8_debug_gemm_mx_wait_limit.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, u64, vp]
-        L.fp8_debug_wait_probe.restype = i32
-        L.fp8_debug_wait_probe.argtypes = [vp, u64, vp]
-        L.fp8_launch_count.restype = u64
-        L.fp8_launch_count.argtypes = []
-        _lib = L
+        _lib = load(LIB_PATH)
     return _lib
+
+
+def load(path: str):
+    """A ctypes handle on a build of the library at `path`, signatures declared."""
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    i64, u64, i32, vp, sz = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    L.fp8_status_string.restype = ctypes.c_char_p
+    L.fp8_status_string.argtypes = [i32]
+    L.fp8_scales_bytes.restype = sz
+    L.fp8_scales_bytes.argtypes = [i64, i64, i32, i32]
+    L.fp8_quantize_workspace_bytes.restype = sz
+    L.fp8_quantize_workspace_bytes.argtypes = [i64, i64, i32]
+    L.fp8_quantize.restype = i32
+    L.fp8_quantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp, vp, sz, vp]
+    L.fp8_quantize_tensor_noalloc.restype = i32
+    L.fp8_quantize_tensor_noalloc.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, vp]
+    L.fp8_quantize_delayed.restype = i32
+    L.fp8_quantize_delayed.argtypes = [vp, i64, i64, i64, i32, vp, i32, i32, i32, vp, i64, vp, vp]
+    L.fp8_dequantize.restype = i32
+    L.fp8_dequantize.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, i64, vp]
+    L.fp8_gemm_blockscaled.restype = i32
+    L.fp8_gemm_blockscaled.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp, vp]
+    L.fp8_gemm_blockscaled_quantized_out.restype = i32
+    L.fp8_gemm_blockscaled_quantized_out.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp]
+    L.fp8_gemm_mx.restype = i32
+    L.fp8_gemm_mx.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
+    L.fp8_nvfp4_scales_bytes.restype = sz
+    L.fp8_nvfp4_scales_bytes.argtypes = [i64, i64, i32]
+    L.fp8_quantize_nvfp4.restype = i32
+    L.fp8_quantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, i64, vp, vp, vp, sz, vp]
+    L.fp8_dequantize_nvfp4.restype = i32
+    L.fp8_dequantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp]
+    L.fp8_gemm_nvfp4.restype = i32
+    L.fp8_gemm_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    L.fp8_debug_gemm_blockscaled_pairs.restype = i32
+    L.fp8_debug_gemm_blockscaled_pairs.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
+    L.fp8_debug_encode_e2m1_f32.restype = i32
+    L.fp8_debug_encode_e2m1_f32.argtypes = [vp, i64, vp, vp]
+    L.fp8_debug_encode_f32.restype = i32
+    L.fp8_debug_encode_f32.argtypes = [vp, i64, i32, vp, vp]
+    L.fp8_debug_gemm_blockscaled_wait_limit.restype = i32
+    L.fp8_debug_gemm_blockscaled_wait_limit.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i64, i64, i64, vp,
+                                                         u64, vp]
+    L.fp8_debug_gemm_mx_wait_limit.restype = i32
+    L.fp8_debug_gemm_mx_wait_limit.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, u64, vp]
+    L.fp8_debug_wait_probe.restype = i32
+    L.fp8_debug_wait_probe.argtypes = [vp, u64, vp]
+    L.fp8_launch_count.restype = u64
+    L.fp8_launch_count.argtypes = []
+    L.fp8_debug_oob_read.restype = u64
+    L.fp8_debug_oob_read.argtypes = []
+    L.fp8_debug_checked_build.restype = i32
+    L.fp8_debug_checked_build.argtypes = []
+    return L
 
 
 def declared_functions() -> list[str]:

@@ -16,6 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8bs.so")
+# the same library with every plain global store of its kernels bounds-checked
+# (-DFP8BS_CHECK; see csrc/check.cuh): a test build, not the product path
+CHECK_LIB = os.path.join(HERE, "libfp8bs_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE division/sqrt and no flush-to-zero: the scales must round exactly like
@@ -42,22 +45,25 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, check: bool = False) -> str:
+    """Build libfp8bs.so (or, with check=True, libfp8bs_check.so); returns its path."""
+    lib = CHECK_LIB if check else LIB
+    if not force and up_to_date(lib):
+        return lib
+    bdir = os.path.join(BUILD_DIR, "check") if check else BUILD_DIR
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + (["-DFP8BS_CHECK"] if check else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *NVFLAGS, *extra, "-c", src, "-o", obj]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
@@ -68,14 +74,14 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(sources())) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (p.stdout, p.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose_ptxas="-v" in sys.argv))
+    print(build(force=True, verbose_ptxas="-v" in sys.argv, check="--check" in sys.argv))

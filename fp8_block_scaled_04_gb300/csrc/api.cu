@@ -98,6 +98,22 @@ const char *fp8_status_string(fp8_status_t s) {
 
 uint64_t fp8_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+uint64_t fp8_debug_oob_read(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ~0ull;
+  const uint64_t r[3] = {oob_record_quantize(), oob_record_nvfp4(), oob_record_gemm()};
+  for (uint64_t v : r)
+    if (v != 0) return v;
+  return 0;
+}
+
+int fp8_debug_checked_build(void) {
+#ifdef FP8BS_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 size_t fp8_scales_bytes(int64_t rows, int64_t cols, fp8_gran_t gran, fp8_sf_layout_t sf_layout) {
   if (rows < 0 || cols < 0) return 0;
   switch (gran) {

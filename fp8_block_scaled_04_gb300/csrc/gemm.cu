@@ -43,6 +43,7 @@
 #include "internal.h"
 #include "fp8_math.cuh"
 #include "ptx.cuh"
+#include "check.cuh"
 
 namespace fp8bs {
 namespace {
@@ -77,12 +78,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// Store 32 fp32 values (one row, 32 consecutive columns) as bf16; n_left is
-// the number of valid columns (multiple of 8).
-__device__ __forceinline__ void store_row32(uint16_t *dst, const float (&v)[32], int n_left) {
+// Store 32 fp32 values (one row, 32 consecutive columns) as bf16 at element
+// offset off of out (extent elements); n_left is the number of valid columns
+// (multiple of 8).
+__device__ __forceinline__ void store_row32(uint16_t *out, int64_t off, int64_t extent, const float (&v)[32],
+                                            int n_left) {
+  uint16_t *dst = out + off;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    if (8 * j < n_left) {
+    if (8 * j < n_left && FP8BS_GUARD(off + 8 * j, 8, extent)) {
       uint4 w = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
                            pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
       *reinterpret_cast<uint4 *>(dst + 8 * j) = w;
@@ -269,7 +273,8 @@ __device__ __forceinline__ void fold_epilogue_tma(float2 (&acc)[NA], int m, int 
     }
     float s, s_inv;
     scale_pair(__uint_as_float(mx << 16), vmax_of(QFMT), s, s_inv);
-    if (m < M && n0 < N) q_scales[static_cast<int64_t>(n0 >> 7) * M + m] = s;
+    if (m < M && n0 < N && FP8BS_GUARD(static_cast<int64_t>(n0 >> 7) * M + m, 1, static_cast<int64_t>(N / 128) * M))
+      q_scales[static_cast<int64_t>(n0 >> 7) * M + m] = s;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // 16 codes per chunk
       float f[16];
@@ -971,7 +976,8 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < BX; ++j) {
           const int m = m0 + j;
-          if (m < M) out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+          if (m < M && FP8BS_GUARD(static_cast<int64_t>(m) * N + n, 1, static_cast<int64_t>(M) * N))
+            out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
         }
       }
     }
@@ -1206,7 +1212,8 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < BX; ++j) {
           const int m = m0 + j;
-          if (m < M) out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+          if (m < M && FP8BS_GUARD(static_cast<int64_t>(m) * N + n, 1, static_cast<int64_t>(M) * N))
+            out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
         }
       }
     }
@@ -1552,7 +1559,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c][i]) * s;
           }
-          store_row32(out + static_cast<int64_t>(m) * N + nc, v, N - nc);
+          store_row32(out, static_cast<int64_t>(m) * N + nc, static_cast<int64_t>(M) * N, v, N - nc);
         }
       }
     }
@@ -1775,6 +1782,8 @@ fp8_status_t launch_fold_tiles(const uint8_t *a, const float *sa, const uint8_t 
 }
 
 }  // namespace
+
+FP8BS_OOB_READER(oob_record_gemm)
 
 fp8_status_t launch_gemm_fold(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb, int a_fmt,
                               int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,

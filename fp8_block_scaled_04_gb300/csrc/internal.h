@@ -86,6 +86,12 @@ fp8_status_t launch_gemm_nvfp4(const uint8_t *a, const uint8_t *sfa, const float
                                const uint8_t *sfb, const float *tb, uint16_t *out, int64_t M, int64_t N, int64_t K,
                                int *dev_status, cudaStream_t stream);
 
+// Store-check records of the FP8BS_CHECK build, one per translation unit
+// (0 in the normal build): read and cleared.
+uint64_t oob_record_quantize();
+uint64_t oob_record_nvfp4();
+uint64_t oob_record_gemm();
+
 // 2-D tensor map over a row-major uint8 matrix [rows x cols] (cols contiguous,
 // row stride ld bytes), box = box_cols x box_rows, 128-byte swizzle.
 bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,

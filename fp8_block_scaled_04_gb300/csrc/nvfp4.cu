@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "check.cuh"
 
 namespace fp8bs {
 namespace {
@@ -189,8 +190,11 @@ __global__ void __launch_bounds__(kThreads)
       uint2 p;
       encode_block(v[j][0], v[j][1], bs, c, p);
       if (g < ng) {
-        *reinterpret_cast<uint2 *>(q + r * ldq + g * 8) = p;
-        sf[sf_offset(r, g, ng, tiled)] = static_cast<uint8_t>(c);
+        if (FP8BS_GUARD(r * ldq + g * 8, 8, (rows - 1) * ldq + cols / 2))
+          *reinterpret_cast<uint2 *>(q + r * ldq + g * 8) = p;
+        const int64_t so = sf_offset(r, g, ng, tiled);
+        if (FP8BS_GUARD(so, 1, tiled ? ((rows + 127) / 128) * ((ng + 3) / 4) * 512 : rows * ng))
+          sf[so] = static_cast<uint8_t>(c);
       }
     }
   }
@@ -221,9 +225,11 @@ __global__ void __launch_bounds__(kThreads)
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p) : "f"(b), "f"(a));
         o[4 * h + i] = p;
       }
-    uint4 *dst = reinterpret_cast<uint4 *>(out + r * ldo + g * 16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if (FP8BS_GUARD(r * ldo + g * 16, 16, (rows - 1) * ldo + cols)) {
+      uint4 *dst = reinterpret_cast<uint4 *>(out + r * ldo + g * 16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kThreads)
       lo |= ((c >> (4 * i)) & 15u) << (8 * i);
       hi |= ((c >> (16 + 4 * i)) & 15u) << (8 * i);
     }
-    reinterpret_cast<uint2 *>(out)[t] = make_uint2(lo, hi);
+    if (FP8BS_GUARD(t, 1, n8)) reinterpret_cast<uint2 *>(out)[t] = make_uint2(lo, hi);
   }
 }
 
@@ -255,6 +261,8 @@ int grid_for(int64_t work_items) {
 }
 
 }  // namespace
+
+FP8BS_OOB_READER(oob_record_nvfp4)
 
 fp8_status_t launch_quantize_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, bool tiled,
                                    const float *static_ts, uint8_t *q, int64_t ld_q, uint8_t *sf, float *ts_out,

@@ -25,6 +25,7 @@
 #include "internal.h"
 #include "fp8_math.cuh"
 #include "ptx.cuh"
+#include "check.cuh"
 
 namespace fp8bs {
 namespace {
@@ -105,12 +106,15 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
         const int64_t j = pcv / TPG;
         const int64_t ng = cols / 32;
         uint8_t *sf = static_cast<uint8_t *>(scales);
-        sf[TILED ? mx_tiled_index(r, j, ng) : r * ng + j] = static_cast<uint8_t>(e + 127);
+        const int64_t si = TILED ? mx_tiled_index(r, j, ng) : r * ng + j;
+        if (FP8BS_GUARD(si, 1, TILED ? ((rows + 127) / 128) * ((ng + 3) / 4) * 512 : rows * ng))
+          sf[si] = static_cast<uint8_t>(e + 127);
       }
     } else {
       float s;
       scale_pair(amax, vmax, s, my_inv);
-      if (lane < PAIRS && pcv < vec_per_row) static_cast<float *>(scales)[(pcv / TPG) * rows + r] = s;
+      if (lane < PAIRS && pcv < vec_per_row && FP8BS_GUARD((pcv / TPG) * rows + r, 1, (cols / GROUP) * rows))
+        static_cast<float *>(scales)[(pcv / TPG) * rows + r] = s;
     }
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i) {
@@ -120,7 +124,8 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
       if (cv >= vec_per_row) continue;
       float f[8];
       bf16x8_to_f32(v[i], f);
-      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+      if (FP8BS_GUARD(r * ldq + cv * 8, 8, (rows - 1) * ldq + cols))
+        *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
     }
   }
 }
@@ -206,7 +211,8 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_kernel(const uint16_t *
       if (record_amax != nullptr) rec = max(rec, absmax_bits8(v[i]));
       float f[8];
       bf16x8_to_f32(v[i], f);
-      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+      if (FP8BS_GUARD(r * ldq + cv * 8, 8, (rows - 1) * ldq + cols))
+        *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
     }
   }
   if (record_amax != nullptr) {
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) delayed_scale_kernel(float *__restri
       s = __fdiv_rn(scaled, vmax_of(fmt));
     }
     *scale_out = s;
-    history[slot] = 0.0f;
+    if (FP8BS_GUARD(slot, 1, hlen)) history[slot] = 0.0f;
   }
 }
 
@@ -296,14 +302,15 @@ __global__ void __launch_bounds__(kThreads) quant_token_kernel(const uint16_t *_
   for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
   float s, s_inv;
   scale_pair(__uint_as_float(b << 16), vmax_of(FMT), s, s_inv);
-  if (threadIdx.x == 0) scales[r] = s;
+  if (threadIdx.x == 0 && FP8BS_GUARD(r, 1, gridDim.x)) scales[r] = s;
 #pragma unroll
   for (int i = 0; i < U; ++i) {
     const int64_t cv = threadIdx.x + static_cast<int64_t>(i) * kThreads;
     if (cv < vec_per_row) {
       float f[8];
       bf16x8_to_f32(v[i], f);
-      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+      if (FP8BS_GUARD(r * ldq + cv * 8, 8, (static_cast<int64_t>(gridDim.x) - 1) * ldq + cols))
+        *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
     }
   }
 }
@@ -329,11 +336,12 @@ __global__ void __launch_bounds__(kThreads) quant_token_long_kernel(const uint16
   for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
   float s, s_inv;
   scale_pair(__uint_as_float(b << 16), vmax_of(FMT), s, s_inv);
-  if (threadIdx.x == 0) scales[r] = s;
+  if (threadIdx.x == 0 && FP8BS_GUARD(r, 1, gridDim.x)) scales[r] = s;
   for (int64_t cv = threadIdx.x; cv < vec_per_row; cv += kThreads) {
     float f[8];
     bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xr + cv * 8), f);
-    *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
+    if (FP8BS_GUARD(r * ldq + cv * 8, 8, (static_cast<int64_t>(gridDim.x) - 1) * ldq + cols))
+      *reinterpret_cast<uint2 *>(q + r * ldq + cv * 8) = encode8<FMT>(f, s_inv);
   }
 }
 
@@ -364,14 +372,16 @@ __global__ void __launch_bounds__(kThreads) quant_block_kernel(const uint16_t *_
   for (int w = 0; w < kThreads / 32; ++w) b = max(b, red[w]);
   float s, s_inv;
   scale_pair(__uint_as_float(b << 16), vmax_of(FMT), s, s_inv);
-  if (threadIdx.x == 0) scales[rb * (cols / 128) + kb] = s;
+  if (threadIdx.x == 0 && FP8BS_GUARD(rb * (cols / 128) + kb, 1, ((rows + 127) / 128) * (cols / 128)))
+    scales[rb * (cols / 128) + kb] = s;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t r = rb * 128 + r0 + 16 * i;
     if (r < rows) {
       float f[8];
       bf16x8_to_f32(v[i], f);
-      *reinterpret_cast<uint2 *>(q + r * ldq + kb * 128 + cvl * 8) = encode8<FMT>(f, s_inv);
+      if (FP8BS_GUARD(r * ldq + kb * 128 + cvl * 8, 8, (rows - 1) * ldq + cols))
+        *reinterpret_cast<uint2 *>(q + r * ldq + kb * 128 + cvl * 8) = encode8<FMT>(f, s_inv);
     }
   }
 }
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kThreads) channel_quant_kernel(const uint16_t 
   for (int j = 0; j < 8; ++j) {
     float s;
     scale_pair(__uint_as_float(col_amax[v * 8 + j]), vmax_of(FMT), s, s_inv[j]);
-    if (blockIdx.y == 0 && slab == 0) scales[v * 8 + j] = s;
+    if (blockIdx.y == 0 && slab == 0 && FP8BS_GUARD(v * 8 + j, 1, cols)) scales[v * 8 + j] = s;
   }
   // this thread's rows r0 + slab + slabs * k, k = 0 .. n-1, taken from the last
   if (r0 + slab >= r1) return;
@@ -501,7 +511,8 @@ __global__ void __launch_bounds__(kThreads) channel_quant_kernel(const uint16_t 
       bf16x8_to_f32(vv[i], f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], s_inv[j]);
-      *reinterpret_cast<uint2 *>(q + (r0 + slab + k * g.slabs) * ldq + v * 8) = encode8<FMT>(f, 1.0f);
+      if (FP8BS_GUARD((r0 + slab + k * g.slabs) * ldq + v * 8, 8, (rows - 1) * ldq + cols))
+        *reinterpret_cast<uint2 *>(q + (r0 + slab + k * g.slabs) * ldq + v * 8) = encode8<FMT>(f, 1.0f);
     }
   }
 }
@@ -566,9 +577,11 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__rest
           o[2 * j + h] = blo | (bhi << 16);
         }
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(out + r * ldo + c);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      if (FP8BS_GUARD(r * ldo + c, 16, (rows - 1) * ldo + cols)) {
+        uint4 *dst = reinterpret_cast<uint4 *>(out + r * ldo + c);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
     }
   }
 }
@@ -584,7 +597,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_kernel(const float *__res
     const float4 a = reinterpret_cast<const float4 *>(x)[2 * i];
     const float4 b = reinterpret_cast<const float4 *>(x)[2 * i + 1];
     const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    reinterpret_cast<uint2 *>(out)[i] = encode8<FMT>(f, 1.0f);
+    if (FP8BS_GUARD(i, 1, n8)) reinterpret_cast<uint2 *>(out)[i] = encode8<FMT>(f, 1.0f);
   }
 }
 
@@ -596,6 +609,8 @@ int stream_grid(int64_t tasks) {
 }
 
 }  // namespace
+
+FP8BS_OOB_READER(oob_record_quantize)
 
 fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, int gran,
                              int sf_layout, const float *static_scale, uint8_t *q, int64_t ld_q, void *scales,

@@ -342,6 +342,18 @@ fp8_status_t fp8_debug_gemm_mx_wait_limit(const void *a_dev, const uint8_t *a_sf
                                           void *out_dev, int64_t M, int64_t N, int64_t K, int *dev_status,
                                           uint64_t wait_ns, fp8_stream_t stream);
 
+/* Store checks (no counterpart on the pages; a stand-in for a memory checker):
+ * a library built with -DFP8BS_CHECK (libfp8bs_check.so) checks, before every
+ * plain global store of its kernels, that the store stays inside the extent the
+ * call's shape gives the buffer; a store outside it is skipped and the first one
+ * is recorded as (source line << 40) | (element offset & (2^40 - 1)). (TMA
+ * stores are clipped to their tensor maps by the hardware.) fp8_debug_oob_read
+ * synchronises the current device, returns the record (0: no violation) and
+ * clears it; in the normal build its kernels carry no checks and it returns 0.
+ * fp8_debug_checked_build returns 1 for the checked build, else 0. */
+uint64_t fp8_debug_oob_read(void);
+int fp8_debug_checked_build(void);
+
 /* Number of kernel launches the library has enqueued since it was loaded
  * (all entry points, all devices); a diagnostic counter. */
 uint64_t fp8_launch_count(void);
