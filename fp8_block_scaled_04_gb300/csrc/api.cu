@@ -47,7 +47,8 @@ int device_sm_count() {
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 static bool make_tmap_2d(void *tmap_out, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base,
-                        uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows, uint32_t box_cols) {
+                        uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows, uint32_t box_cols,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -62,7 +63,7 @@ static bool make_tmap_2d(void *tmap_out, CUtensorMapDataType dtype, uint32_t ele
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(static_cast<CUtensorMap *>(tmap_out), dtype, 2, const_cast<void *>(base), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -75,6 +76,12 @@ bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols
 bool make_tmap_u16(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
                    uint32_t box_cols) {
   return make_tmap_2d(tmap_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, rows, cols, ld, box_rows, box_cols);
+}
+
+bool make_tmap_f32(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                   uint32_t box_cols) {
+  return make_tmap_2d(tmap_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, ld, box_rows, box_cols,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace fp8bs

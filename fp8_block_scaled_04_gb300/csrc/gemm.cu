@@ -121,6 +121,14 @@ __device__ __forceinline__ void store_row32(uint16_t *out, int64_t off, int64_t 
 #define FOLD_MMA_ISSUERS 2  // threads (in warps 1..) issuing the fold kernels' MMAs, k-blocks dealt round robin
 #endif
 
+#ifndef SWAP_MMA_ISSUERS
+#define SWAP_MMA_ISSUERS 2  // decode kernel: threads (in warps 1..) issuing its MMAs, k-blocks dealt round robin
+#endif
+
+#ifndef SWAP_FOLD_COLS
+#define SWAP_FOLD_COLS 16  // decode kernel: activation rows per fold warp (16 or 32)
+#endif
+
 #ifndef FOLD_CHUNK
 #define FOLD_CHUNK 64  // tensor-memory columns per fold load (16 or 32: pipelined; 64: one round trip per half)
 #endif
@@ -794,25 +802,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
 // =====================================================================
 // D[n, m] = sum_k W[n, k] X[m, k]: the MMA's M side is 128 rows of W (one
 // 128x128 weight block per K chunk, so one weight scale per chunk), its N side
-// is BX rows of X. Each fold thread owns one W row and BX accumulators; the
-// activation scales s_x[kb, m] vary along its row and are broadcast by shuffles.
+// is BX rows of X. Each fold thread owns one W row and BXW = BX / G of the BX
+// activation rows (G groups of four fold warps, BXW = SWAP_FOLD_COLS: with
+// all 64 rows per warp the fold warps, not HBM, set the k-block rate); the
+// activation scales s_x[kb, m] vary along its row and reach every lane as
+// shared-memory broadcasts. Two threads issue the MMAs, alternate k-blocks.
 template <int BX, int STAGES>
 struct SwapCfg {
   static constexpr int W_BYTES = BM * BK;
   static constexpr int X_BYTES = BX * BK;
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
   static constexpr int NBUF = 4;                       // tensor-memory partial buffers
-  static constexpr int THREADS = 32 * (2 + 4);
+  static constexpr int G = BX > SWAP_FOLD_COLS ? BX / SWAP_FOLD_COLS : 1;  // fold warp groups
+  static constexpr int BXW = BX / G;                   // activation rows per fold warp
+  static constexpr int FOLD_WARPS = 4 * G;
+  static constexpr int ISSUERS = SWAP_MMA_ISSUERS;      // MMA-issuing warps 1 .. ISSUERS
+  static constexpr int FIRST_FOLD_WARP = 1 + ISSUERS;
+  static constexpr int THREADS = 32 * (FIRST_FOLD_WARP + FOLD_WARPS);
+  static_assert(ISSUERS >= 1 && ISSUERS <= 2 && NBUF % ISSUERS == 0, "each partial buffer needs one issuer");
   static constexpr uint32_t TMEM_COLS = NBUF * BX <= 32 ? 32 : (NBUF * BX <= 64 ? 64 : (NBUF * BX <= 128 ? 128 : 256));
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  static constexpr int CBUF_BYTES = FOLD_WARPS * 2 * BXW * 4;   // per fold warp: two slots of BXW fp32 products
+  static constexpr int OTILE_BYTES = FOLD_WARPS * BXW * 32 * 2;  // per fold warp: 32 columns x BXW rows, bf16
+  // scale chunks (when the scales' layout allows tensor copies): two slots,
+  // each KBC k-blocks of s_x[kb, tile's BX rows] followed by s_w[tile, kb]
+  static constexpr int KBC = BX >= 64 ? 28 : 64;
+  static constexpr int SC_X_BYTES = KBC * BX * 4;
+  static constexpr int SC_W_OFF = SC_X_BYTES / 4;                  // in floats
+  static constexpr int SC_SLOT_BYTES = SC_X_BYTES + ((KBC * 4 + 127) / 128) * 128;
+  static constexpr int SC_TX_BYTES = SC_X_BYTES + KBC * 4;          // the two boxes' bytes
+  static constexpr int SC_OFFSET = STAGES * STAGE_BYTES + CBUF_BYTES + OTILE_BYTES;
+  static constexpr int SMEM = SC_OFFSET + 2 * SC_SLOT_BYTES + 1024;
+  static_assert(KBC % 4 == 0 && KBC <= 256 && SC_X_BYTES % 128 == 0 && SC_OFFSET % 128 == 0, "scale chunk layout");
   static_assert(BX % 16 == 0 && BX <= 64, "MMA N side");
+  static_assert(SMEM + 256 <= 232448, "shared memory budget");
 };
 
 template <int BX, int STAGES>
 __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
     gemm_fold_swap_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                          const float *__restrict__ sa, const float *__restrict__ sb, uint16_t *__restrict__ out,
-                          int M, int N, int K, uint32_t idesc, int *dev_status, uint64_t wait_ns) {
+                          const __grid_constant__ CUtensorMap tmSX, const __grid_constant__ CUtensorMap tmSW,
+                          int sc_tma, const float *__restrict__ sa, const float *__restrict__ sb,
+                          uint16_t *__restrict__ out, int M, int N, int K, uint32_t idesc, int *dev_status,
+                          uint64_t wait_ns) {
   using C = SwapCfg<BX, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -820,7 +851,8 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   // stage's next k-block needs the release of k-block kc + NBUF first, and
   // STAGES > NBUF)
   static_assert(STAGES > C::NBUF, "stage barrier parity");
-  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[C::NBUF], drain;
+  // sfull / sempty: the two scale-chunk slots (landed / read by every fold warp)
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[C::NBUF], drain, sfull[2], sempty[2];
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -835,12 +867,20 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < C::NBUF; ++b) mbar_init(&tempty[b], 4);
-    mbar_init(&drain, 1);
+    for (int b = 0; b < C::NBUF; ++b) mbar_init(&tempty[b], C::FOLD_WARPS);
+    mbar_init(&drain, C::ISSUERS);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&sfull[j], 1);
+      mbar_init(&sempty[j], C::FOLD_WARPS);
+    }
     ctl.abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW);
+    if (sc_tma) {
+      tma_prefetch_desc(&tmSX);
+      tma_prefetch_desc(&tmSW);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
@@ -860,15 +900,49 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   grid_dependents_launch();
   grid_dependency_wait();
   const uint32_t tmem = ctl.tmem_base;
+  float *scbuf = reinterpret_cast<float *>(smem + C::SC_OFFSET);
 
   if (warp == 0) {
     if (lane == 0) {
-      int it = 0;
+      int it = 0, chunk = 0;
       bool ok = true;
+      // scale chunk: KBC k-blocks of tile t from k-block kb0 into the next slot
+      // (boxes past K or M read as zeros)
+      auto issue_chunk = [&](int t, int kb0) -> bool {
+        const int slot = chunk & 1;
+        if (!mbar_wait(&sempty[slot], ((chunk >> 1) & 1) ^ 1, wait_ns, &ctl.abort)) return false;
+        const int wt = t / num_x, xt = t - wt * num_x;
+        float *dst = scbuf + slot * (C::SC_SLOT_BYTES / 4);
+        mbar_arrive_expect_tx(&sfull[slot], C::SC_TX_BYTES);
+        tma_load_2d(dst, &tmSX, xt * BX, kb0, &sfull[slot]);
+        tma_load_2d(dst + C::SC_W_OFF, &tmSW, kb0, wt, &sfull[slot]);
+        ++chunk;
+        return true;
+      };
+      if (sc_tma && static_cast<int>(blockIdx.x) < ntiles) ok = issue_chunk(blockIdx.x, 0);
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int wt = tile / num_x, xt = tile - wt * num_x;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
+          if (sc_tma) {
+            // the next chunk's copies start halfway through this one: their
+            // slot held the chunk before this one, which the fold warps (at
+            // most STAGES k-blocks behind) have finished by then, and the
+            // copies have half a chunk of k-blocks to land
+            const int c0 = kb - kb % C::KBC;
+            const int clen = min(C::KBC, KB - c0);
+            if (kb == c0 + min(C::KBC / 2, clen - 1)) {
+              int t_next = tile, kb_next = c0 + C::KBC;
+              if (kb_next >= KB) {
+                t_next = tile + static_cast<int>(gridDim.x);
+                kb_next = 0;
+              }
+              if (t_next < ntiles && !issue_chunk(t_next, kb_next)) {
+                ok = false;
+                break;
+              }
+            }
+          }
           if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
@@ -882,14 +956,24 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       if (!ok) {
         flag_abort(&ctl, dev_status);
         drain_stages<STAGES>(full, it);
+        // the last two chunks' copies may still be in flight (an earlier one
+        // has been waited for by the fold warps before its slot was reused)
+        for (int c = chunk > 2 ? chunk - 2 : 0; c < chunk; ++c)
+          mbar_wait(&sfull[c & 1], (c >> 1) & 1, kDrainTimeoutNs, nullptr);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < C::FIRST_FOLD_WARP) {
+    // MMA issuers: issuer j takes the k-blocks with kc % ISSUERS == j (so each
+    // partial buffer is written by one thread and its MMAs stay in order);
+    // one thread's waits, MMAs and commit take about a k-block's worth of HBM
+    // time, so consecutive k-blocks' issue work overlaps
     if (lane == 0) {
+      const int me = warp - 1;
       int it = 0, kc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb, ++it, ++kc) {
+          if (C::ISSUERS > 1 && kc % C::ISSUERS != me) continue;
           const int b = kc % C::NBUF;
           const int s = it % STAGES;
           const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
@@ -913,56 +997,109 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
     }
   } else {
-    const int quarter = warp & 3;
+    constexpr int BXW = C::BXW;
+    const int fw = warp - C::FIRST_FOLD_WARP;  // fold warp 0 .. FOLD_WARPS - 1
+    const int quarter = warp & 3;           // the tensor-memory lanes (W rows) this warp may read
+    const int col0 = (fw / 4) * BXW;        // its activation rows within the tile: col0 .. col0 + BXW - 1
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr int XR = (BX + 31) / 32;  // activation-scale registers per lane
-    int kc = 0;
+    constexpr int XR = (BXW + 31) / 32;  // activation-scale registers per lane
+    // this warp's shared memory: two slots (even / odd k-blocks) of BXW scale
+    // products, and its 32 output columns x BXW rows of bf16 for the epilogue
+    float *cbuf = reinterpret_cast<float *>(smem + STAGES * C::STAGE_BYTES) + fw * 2 * BXW;
+    uint16_t *otile =
+        reinterpret_cast<uint16_t *>(smem + STAGES * C::STAGE_BYTES + C::CBUF_BYTES) + fw * BXW * 32;
+    int kc = 0, chunk = 0;
     bool ok = true;
-    float acc[BX];
+    float2 acc[BXW / 2];  // acc[i] = activation rows col0 + 2i, + 1 of this thread's output column
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       const int wt = tile / num_x, xt = tile - wt * num_x;
-      const int n = wt * BM + quarter * 32 + lane;  // this thread's W row / output column
-      const int m0 = xt * BX;
+      const int m0 = xt * BX + col0;
       const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
 #pragma unroll
-      for (int j = 0; j < BX; ++j) acc[j] = 0.0f;
-      // lane l holds s_x[kb, m0 + 32 r + l] and s_w[kb] in one of two fixed
-      // register slots (even / odd k-blocks), loaded two k-blocks ahead and
-      // reloaded in place; indices are clamped, not predicated, so that no copy
-      // or select waits on a load in flight (values of rows past M are never stored)
+      for (int j = 0; j < BXW / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      // Scales, tensor-copy path (sc_tma): the producer brings s_x and s_w of
+      // KBC k-blocks at a time into a chunk slot; every lane reads them back
+      // as shared-memory broadcasts and forms s_w * s_x itself.
+      // Register path (a layout the tensor copies cannot describe): lane l
+      // holds s_x[kb, m0 + 32 r + l] and s_w[kb] in one of two fixed register
+      // slots (even / odd k-blocks), loaded two k-blocks ahead and reloaded in
+      // place (indices clamped, not predicated, so that no copy or select waits
+      // on a load in flight; values of rows past M are never stored), forms
+      // the products for its rows and leaves them in the warp's slot for this
+      // k-block's parity. Either way each product is the same fp32 multiply.
       auto load_sx = [&](int kbq, float (&dst)[XR]) {
         const int kq = min(kbq, KB - 1);
 #pragma unroll
         for (int r = 0; r < XR; ++r) dst[r] = __ldg(sa + static_cast<int64_t>(kq) * M + min(m0 + 32 * r + lane, M - 1));
       };
-      float xs0[XR], xs1[XR];
-      load_sx(0, xs0);
-      load_sx(1, xs1);
-      float ws0 = __ldg(sb_blk), ws1 = __ldg(sb_blk + (KB > 1 ? 1 : 0));
+      float xs0[XR], xs1[XR], ws0 = 0.0f, ws1 = 0.0f;
+      if (!sc_tma) {
+        load_sx(0, xs0);
+        load_sx(1, xs1);
+        ws0 = __ldg(sb_blk);
+        ws1 = __ldg(sb_blk + (KB > 1 ? 1 : 0));
+      }
       auto fold_one = [&](int kb, float (&xs)[XR], float &ws) -> bool {
         const int b = kc % C::NBUF;
-        // lane l forms s_w * s_x for activation rows l (+ 32 r) once; the
-        // shuffles then carry finished products (same fp32 multiply)
-        float cs[XR];
+        const int kl = kb % C::KBC;
+        const float *sxc = scbuf + (chunk & 1) * (C::SC_SLOT_BYTES / 4);
+        if (sc_tma) {
+          if (kl == 0) {
+            const bool landed = mbar_wait(&sfull[chunk & 1], (chunk >> 1) & 1, wait_ns, &ctl.abort);
+            if (!__all_sync(0xffffffffu, landed)) return false;
+          }
+        } else {
+          // the slot is rewritten two k-blocks later, after the __syncwarp
+          // that follows this k-block's reads in every lane
+          float *cs = cbuf + (kc & 1) * BXW;
 #pragma unroll
-        for (int q = 0; q < XR; ++q) cs[q] = ws * xs[q];
-        load_sx(kb + 2, xs);
-        ws = __ldg(sb_blk + min(kb + 2, KB - 1));
+          for (int q = 0; q < XR; ++q)
+            if (32 * q + lane < BXW) cs[32 * q + lane] = ws * xs[q];
+          load_sx(kb + 2, xs);
+          ws = __ldg(sb_blk + min(kb + 2, KB - 1));
+          __syncwarp();
+        }
         const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, wait_ns, &ctl.abort);
         if (!__all_sync(0xffffffffu, got)) return false;
         tc_fence_after();
-        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
-        // the whole BX-column partial in one load and one wait
-        uint32_t r[BX];
-        tmem_ld_chunk<BX>(taddr, r);
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX + col0);
+        // the warp's BXW columns of the partial in one load and one wait
+        uint32_t r[BXW];
+        tmem_ld_chunk<BXW>(taddr, r);
         tmem_wait_ld_regs(r);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
+        if (sc_tma) {
+          const float w = sxc[C::SC_W_OFF + kl];
+          const float2 w2 = make_float2(w, w);
+          const float4 *x4 = reinterpret_cast<const float4 *>(sxc + kl * BX + col0);
 #pragma unroll
-        for (int j = 0; j < BX; ++j) {
-          const float sc = __shfl_sync(0xffffffffu, cs[j / 32], j % 32);
-          acc[j] = fmaf(sc, __uint_as_float(r[j]), acc[j]);
+          for (int i = 0; i < BXW / 4; ++i) {
+            const float4 xv = x4[i];
+            acc[2 * i] = __ffma2_rn(__fmul2_rn(w2, make_float2(xv.x, xv.y)),
+                                    make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), acc[2 * i]);
+            acc[2 * i + 1] = __ffma2_rn(__fmul2_rn(w2, make_float2(xv.z, xv.w)),
+                                        make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])),
+                                        acc[2 * i + 1]);
+          }
+          if (kl == C::KBC - 1 || kb == KB - 1) {
+            // this chunk's scales are read (the products above consumed them)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sempty[chunk & 1]);
+            ++chunk;
+          }
+        } else {
+          const float4 *c4 = reinterpret_cast<const float4 *>(cbuf + (kc & 1) * BXW);
+#pragma unroll
+          for (int i = 0; i < BXW / 4; ++i) {
+            const float4 c = c4[i];
+            acc[2 * i] = __ffma2_rn(make_float2(c.x, c.y),
+                                    make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), acc[2 * i]);
+            acc[2 * i + 1] = __ffma2_rn(make_float2(c.z, c.w),
+                                        make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])),
+                                        acc[2 * i + 1]);
+          }
         }
         ++kc;
         return true;
@@ -972,14 +1109,25 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         if (ok && kb + 1 < KB) ok = fold_one(kb + 1, xs1, ws1);
       }
       if (!ok) break;
-      if (n < N) {
+      // the warp's 32 columns x BXW rows go through shared memory so that each
+      // output row's 64 bytes leave in four 16-byte stores (eight rows per
+      // warp-wide store) instead of 32 two-byte ones
 #pragma unroll
-        for (int j = 0; j < BX; ++j) {
-          const int m = m0 + j;
-          if (m < M && FP8BS_GUARD(static_cast<int64_t>(m) * N + n, 1, static_cast<int64_t>(M) * N))
-            out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
-        }
+      for (int j = 0; j < BXW / 2; ++j) {
+        otile[(2 * j) * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j].x));
+        otile[(2 * j + 1) * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j].y));
       }
+      __syncwarp();
+      const int ncol = wt * BM + quarter * 32 + (lane & 3) * 8;  // N % 16 == 0: a chunk is all in or all out
+#pragma unroll
+      for (int i = 0; i < BXW / 8; ++i) {
+        const int j = 8 * i + (lane >> 2);
+        const int m = m0 + j;
+        if (m < M && ncol < N && FP8BS_GUARD(static_cast<int64_t>(m) * N + ncol, 8, static_cast<int64_t>(M) * N))
+          *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(m) * N + ncol) =
+              *reinterpret_cast<const uint4 *>(otile + j * 32 + (lane & 3) * 8);
+      }
+      __syncwarp();  // the next tile rewrites the slot
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
   }
@@ -1700,9 +1848,18 @@ fp8_status_t launch_fold_swap(const uint8_t *a, const float *sa, const uint8_t *
   using C = SwapCfg<BX, ST>;
   auto kern = gemm_fold_swap_kernel<BX, ST>;
   if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+  // the scales by tensor copies when their rows are whole 16-byte units:
+  // s_x as [K/128 rows x M], s_w as [N/128 blocks x K/128]
+  const int64_t KB = K / BK;
+  CUtensorMap tsx = tx, tsw = tx;  // not read on the register path
+  int sc_tma = M % 4 == 0 && KB % 4 == 0 && reinterpret_cast<uintptr_t>(sa) % 16 == 0 &&
+               reinterpret_cast<uintptr_t>(sb) % 16 == 0;
+  if (sc_tma && (!make_tmap_f32(&tsx, sa, KB, M, M, C::KBC, BX) ||
+                 !make_tmap_f32(&tsw, sb, (N + BM - 1) / BM, KB, KB, 1, C::KBC)))
+    return FP8_ERR_CUDA;
   if (launch_dependent(kern, static_cast<unsigned>(persistent_grid(ntiles)), C::THREADS, C::SMEM, stream, tx, tw,
-                       sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), idesc, dev_status,
-                       wait_ns) != cudaSuccess)
+                       tsx, tsw, sc_tma, sa, sb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                       idesc, dev_status, wait_ns) != cudaSuccess)
     return FP8_ERR_CUDA;
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;

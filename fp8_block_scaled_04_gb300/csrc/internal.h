@@ -100,5 +100,10 @@ bool make_tmap_u8(void *tmap_out, const void *base, uint64_t rows, uint64_t cols
 // box's inner extent box_cols x 2 bytes must be at most 128 bytes.
 bool make_tmap_u16(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
                    uint32_t box_cols);
+// The same over a row-major fp32 matrix, unswizzled (scale vectors): ld in
+// elements, a multiple of 4; the box's inner extent box_cols x 4 bytes a
+// multiple of 16; elements outside the matrix read as zero.
+bool make_tmap_f32(void *tmap_out, const void *base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+                   uint32_t box_cols);
 
 }  // namespace fp8bs

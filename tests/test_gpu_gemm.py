@@ -95,6 +95,51 @@ def test_decode_split_k(M, N, K):
     assert tol.bad == 0, tol
 
 
+@pytest.mark.parametrize("M,N,K", [(64, 18432, 8192), (60, 18432, 3584), (61, 18432, 2048), (32, 18448, 7040),
+                                   (16, 20480, 3584), (48, 20608, 8192), (3, 18432, 1024)])
+def test_decode_every_sm_busy(M, N, K):
+    """The decode kernel when the weight blocks fill the GPU (no K split): scales
+    brought by tensor copies in chunks of k-blocks (whole chunks, a partial last
+    chunk, activation rows past M read as zero, several tiles per CTA, a ragged
+    N edge) and by per-lane loads where the copies cannot describe them
+    (M % 4 != 0, K/128 % 4 != 0)."""
+    x = synth.bf16_matrix(M, K, 1.0, 80 + M, 81 + K, 0.01, 50.0)
+    w = synth.bf16_matrix(N, K, 0.02, 82 + N)
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    out = _run_blockscaled(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128)
+    cols = np.unique(np.concatenate([np.arange(0, N, 97), np.arange(N - 140, N)]))
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, cols=cols)
+    tol = within_tolerance(out_f64(out)[:, cols], ref, bound)
+    assert tol.bad == 0, tol
+
+
+def test_decode_scale_paths_agree_bit_for_bit():
+    """The same decode GEMM with its scale vectors 16-byte aligned (tensor-copy
+    path) and shifted by one float (per-lane load path) gives identical bytes:
+    both form each product s_w * s_x with the same fp32 multiply."""
+    M, N, K = 64, 18432, 3584
+    x = synth.bf16_matrix(M, K, 1.0, 90, 91, 0.01, 50.0)
+    w = synth.bf16_matrix(N, K, 0.02, 92)
+    qa, sa, qb, sb = _quant_pair(x, w, fb.TILE_1x128, fb.BLOCK_128x128)
+    a, b = torch.from_numpy(qa).cuda(), torch.from_numpy(qb).cuda()
+    outs = []
+    for shift in (0, 1):
+        sa_d = torch.zeros(sa.size + 4, dtype=torch.float32, device="cuda")[shift:shift + sa.size]
+        sb_d = torch.zeros(sb.size + 4, dtype=torch.float32, device="cuda")[shift:shift + sb.size]
+        sa_d.copy_(torch.from_numpy(sa))
+        sb_d.copy_(torch.from_numpy(sb))
+        assert (sa_d.data_ptr() % 16 == 0) == (shift == 0)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        outs.append(fb.gemm_blockscaled(a, sa_d, fb.TILE_1x128, b, sb_d, fb.BLOCK_128x128, status=status))
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    cols = np.arange(0, N, 61)
+    ref, bound = oracle.gemm(qa, sa, fb.TILE_1x128, qb, sb, fb.BLOCK_128x128, cols=cols)
+    tol = within_tolerance(out_f64(outs[0])[:, cols], ref, bound)
+    assert tol.bad == 0, tol
+
+
 def test_decode_split_k_small_integers_exact():
     """Split-K partial sums of integer-valued operands with power-of-two scales are exact."""
     rng = np.random.default_rng(11)
