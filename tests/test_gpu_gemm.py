@@ -96,7 +96,8 @@ def test_decode_split_k(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 18432, 8192), (60, 18432, 3584), (61, 18432, 2048), (32, 18448, 7040),
-                                   (16, 20480, 3584), (48, 20608, 8192), (3, 18432, 1024)])
+                                   (16, 20480, 3584), (48, 20608, 8192), (3, 18432, 1024),
+                                   (16, 17536, 16896)])
 def test_decode_every_sm_busy(M, N, K):
     """The decode kernel when the weight blocks fill the GPU (no K split): scales
     brought by tensor copies in chunks of k-blocks (whole chunks, a partial last
