@@ -1155,10 +1155,19 @@ struct SwapSplitCfg {
   static constexpr int X_BYTES = BX * BK;
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
   static constexpr int NBUF = 4;                       // tensor-memory partial buffers
-  static constexpr int THREADS = 32 * (2 + 4);
+  // fold warps, MMA issuers and the per-warp shared memory as in SwapCfg
+  static constexpr int G = BX > SWAP_FOLD_COLS ? BX / SWAP_FOLD_COLS : 1;
+  static constexpr int BXW = BX / G;
+  static constexpr int FOLD_WARPS = 4 * G;
+  static constexpr int ISSUERS = SWAP_MMA_ISSUERS;
+  static constexpr int FIRST_FOLD_WARP = 1 + ISSUERS;
+  static constexpr int THREADS = 32 * (FIRST_FOLD_WARP + FOLD_WARPS);
+  static_assert(ISSUERS >= 1 && ISSUERS <= 2 && NBUF % ISSUERS == 0, "each partial buffer needs one issuer");
   static constexpr uint32_t TMEM_COLS = NBUF * BX <= 32 ? 32 : (NBUF * BX <= 64 ? 64 : (NBUF * BX <= 128 ? 128 : 256));
   static constexpr int RED_BYTES = BM * BX * 4;  // this CTA's partial, [BX][128] fp32
-  static constexpr int SMEM = STAGES * STAGE_BYTES + RED_BYTES + 1024;
+  static constexpr int CBUF_BYTES = FOLD_WARPS * 2 * BXW * 4;
+  static constexpr int OTILE_BYTES = FOLD_WARPS * BXW * 32 * 2;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + RED_BYTES + CBUF_BYTES + OTILE_BYTES + 1024;
   static_assert(BX % 16 == 0 && BX <= 64, "MMA N side");
   static_assert(SMEM + 256 <= 232448, "shared memory budget");
 };
@@ -1197,10 +1206,10 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < C::NBUF; ++b) mbar_init(&tempty[b], 4);
-    mbar_init(&drain, 1);
-    mbar_init(&red_full, 4 * (S - 1));  // every fold warp of every other CTA
-    mbar_init(&red_done, 4);                        // the leader's fold warps
+    for (int b = 0; b < C::NBUF; ++b) mbar_init(&tempty[b], C::FOLD_WARPS);
+    mbar_init(&drain, C::ISSUERS);
+    mbar_init(&red_full, C::FOLD_WARPS * (S - 1));  // every fold warp of every other CTA
+    mbar_init(&red_done, C::FOLD_WARPS);            // the leader's fold warps
     ctl.abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmX);
@@ -1245,12 +1254,15 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
         drain_stages<STAGES>(full, it);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < C::FIRST_FOLD_WARP) {
+    // MMA issuers, alternate k-blocks (as in the unsplit kernel)
     if (lane == 0) {
+      const int me = warp - 1;
       int it = 0, kc = 0;
       bool ok = true;
       for (int tile = first_tile; tile < ntiles && ok; tile += tile_step) {
         for (int kb = kb_lo; kb < kb_hi; ++kb, ++it, ++kc) {
+          if (C::ISSUERS > 1 && kc % C::ISSUERS != me) continue;
           const int b = kc % C::NBUF;
           const int s = it % STAGES;
           const uint32_t w0 = smem_u32(smem + s * C::STAGE_BYTES);
@@ -1274,21 +1286,26 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
       mbar_wait(&drain, 0, kDrainTimeoutNs, nullptr);
     }
   } else {
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // this thread's W row within the tile
+    constexpr int BXW = C::BXW;
+    const int fw = warp - C::FIRST_FOLD_WARP;  // fold warp 0 .. FOLD_WARPS - 1
+    const int quarter = warp & 3;              // the tensor-memory lanes (W rows) this warp may read
+    const int col0 = (fw / 4) * BXW;           // its activation rows within the tile
+    const int row = quarter * 32 + lane;       // this thread's W row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr int XR = (BX + 31) / 32;  // activation-scale registers per lane
+    constexpr int XR = (BXW + 31) / 32;  // activation-scale registers per lane
     float *red = reinterpret_cast<float *>(smem + STAGES * C::STAGE_BYTES);  // [BX][128]
+    float *cbuf = reinterpret_cast<float *>(smem + STAGES * C::STAGE_BYTES + C::RED_BYTES) + fw * 2 * BXW;
+    uint16_t *otile = reinterpret_cast<uint16_t *>(smem + STAGES * C::STAGE_BYTES + C::RED_BYTES + C::CBUF_BYTES) +
+                      fw * BXW * 32;
     int kc = 0, tn = 0;
     bool ok = true;
-    float acc[BX];
+    float acc[BXW];
     for (int tile = first_tile; tile < ntiles && ok; tile += tile_step, ++tn) {
       const int wt = tile / num_x, xt = tile - wt * num_x;
-      const int n = wt * BM + row;  // this thread's output column
-      const int m0 = xt * BX;
+      const int m0 = xt * BX + col0;
       const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
 #pragma unroll
-      for (int j = 0; j < BX; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < BXW; ++j) acc[j] = 0.0f;
       // scale slots as in the unsplit kernel, over this CTA's k-blocks [kb_lo, kb_hi)
       auto load_sx = [&](int kbq, float (&dst)[XR]) {
         const int kq = min(kbq, kb_hi - 1);
@@ -1301,26 +1318,33 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
       float ws0 = __ldg(sb_blk + kb_lo), ws1 = __ldg(sb_blk + min(kb_lo + 1, kb_hi - 1));
       auto fold_one = [&](int kb, float (&xs)[XR], float &ws) -> bool {
         const int b = kc % C::NBUF;
-        float cs[XR];
+        // products in the warp's slot for this k-block's parity, read back as
+        // broadcasts (as in the unsplit kernel's register path)
+        float *cs = cbuf + (kc & 1) * BXW;
 #pragma unroll
-        for (int q = 0; q < XR; ++q) cs[q] = ws * xs[q];
+        for (int q = 0; q < XR; ++q)
+          if (32 * q + lane < BXW) cs[32 * q + lane] = ws * xs[q];
         load_sx(kb + 2, xs);
         ws = __ldg(sb_blk + min(kb + 2, kb_hi - 1));
+        __syncwarp();
         const bool got = mbar_wait(&empty[kc % STAGES], (kc / STAGES) & 1, kWaitTimeoutNs, &ctl.abort);
         if (!__all_sync(0xffffffffu, got)) return false;
         tc_fence_after();
-        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX);
-        // the whole BX-column partial in one load and one wait
-        uint32_t r[BX];
-        tmem_ld_chunk<BX>(taddr, r);
+        const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(b * BX + col0);
+        uint32_t r[BXW];
+        tmem_ld_chunk<BXW>(taddr, r);
         tmem_wait_ld_regs(r);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
+        const float4 *c4 = reinterpret_cast<const float4 *>(cs);
 #pragma unroll
-        for (int j = 0; j < BX; ++j) {
-          const float sc = __shfl_sync(0xffffffffu, cs[j / 32], j % 32);
-          acc[j] = fmaf(sc, __uint_as_float(r[j]), acc[j]);
+        for (int i = 0; i < BXW / 4; ++i) {
+          const float4 c = c4[i];
+          acc[4 * i + 0] = fmaf(c.x, __uint_as_float(r[4 * i + 0]), acc[4 * i + 0]);
+          acc[4 * i + 1] = fmaf(c.y, __uint_as_float(r[4 * i + 1]), acc[4 * i + 1]);
+          acc[4 * i + 2] = fmaf(c.z, __uint_as_float(r[4 * i + 2]), acc[4 * i + 2]);
+          acc[4 * i + 3] = fmaf(c.w, __uint_as_float(r[4 * i + 3]), acc[4 * i + 3]);
         }
         ++kc;
         return true;
@@ -1335,7 +1359,7 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
         if (rank != 0) {
           // leave this CTA's partial for the leader and wait until it has been read
 #pragma unroll
-          for (int j = 0; j < BX; ++j) red[j * BM + row] = acc[j];
+          for (int j = 0; j < BXW; ++j) red[(col0 + j) * BM + row] = acc[j];
           __syncwarp();
           if (lane == 0) mbar_arrive_release_cluster(cluster_addr(&red_full, 0));
           const bool done = mbar_wait(&red_done, phase, kWaitTimeoutNs, &ctl.abort);
@@ -1350,20 +1374,27 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
         for (int p = 1; p < S; ++p) {
           const uint32_t base = cluster_addr(red, static_cast<uint32_t>(p)) + 4u * static_cast<uint32_t>(row);
 #pragma unroll
-          for (int j = 0; j < BX; ++j) acc[j] += ld_shared_cluster_f32(base + 4u * static_cast<uint32_t>(j * BM));
+          for (int j = 0; j < BXW; ++j)
+            acc[j] += ld_shared_cluster_f32(base + 4u * static_cast<uint32_t>((col0 + j) * BM));
         }
         __syncwarp();
         if (lane == 0)
           for (int p = 1; p < S; ++p) mbar_arrive_release_cluster(cluster_addr(&red_done, static_cast<uint32_t>(p)));
       }
-      if (n < N) {
+      // output through the warp's shared tile, 16-byte row stores (as in the unsplit kernel)
 #pragma unroll
-        for (int j = 0; j < BX; ++j) {
-          const int m = m0 + j;
-          if (m < M && FP8BS_GUARD(static_cast<int64_t>(m) * N + n, 1, static_cast<int64_t>(M) * N))
-            out[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
-        }
+      for (int j = 0; j < BXW; ++j) otile[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+      __syncwarp();
+      const int ncol = wt * BM + quarter * 32 + (lane & 3) * 8;
+#pragma unroll
+      for (int i = 0; i < BXW / 8; ++i) {
+        const int j = 8 * i + (lane >> 2);
+        const int m = m0 + j;
+        if (m < M && ncol < N && FP8BS_GUARD(static_cast<int64_t>(m) * N + ncol, 8, static_cast<int64_t>(M) * N))
+          *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(m) * N + ncol) =
+              *reinterpret_cast<const uint4 *>(otile + j * 32 + (lane & 3) * 8);
       }
+      __syncwarp();
     }
     if (!ok && lane == 0) flag_abort(&ctl, dev_status);
   }
