@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -33,6 +34,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kVecPerLane = 4;                   // 16-byte vectors in flight per lane
 constexpr int kSegVec = 32 * kVecPerLane;        // vectors a warp covers per task (1024 elements)
+// the 1x128 quantizer keeps eight 16-byte loads in flight per lane (measured
+// +3 % over four; it is latency-bound, and the MX kernels' pair layout allows
+// at most four)
+#ifndef FP8BS_TILE_VPL
+#define FP8BS_TILE_VPL 8
+#endif
+constexpr int kTileVecPerLane = FP8BS_TILE_VPL;
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 v;
@@ -49,53 +57,62 @@ __device__ __forceinline__ int64_t mx_tiled_index(int64_t r, int64_t j, int64_t 
 
 // ------------------------------------------------------------ group kernels
 // GROUP elements share a scale (128: 1x128 tile, 32: MX). A warp task is one
-// row segment of kSegVec vectors (4 slots of 32 lanes x 8 elements); groups
+// row segment of 32 * VPL vectors (VPL slots of 32 lanes x 8 elements); groups
 // never straddle rows or lanes. The per-group scale arithmetic (an IEEE
 // division and reciprocal, or the MX exponent) is done once per group: lanes
 // take one (slot, group) pair each, then hand the results back by shuffles.
-template <int v>
-__device__ __forceinline__ uint32_t pick4(const uint32_t (&m)[4], int i) {
-  return i == 0 ? m[0] : (i == 1 ? m[1] : (i == 2 ? m[2] : m[3]));
+// m[i] for a lane-dependent i, by selects (no local-memory array)
+template <int N>
+__device__ __forceinline__ uint32_t pick(const uint32_t (&m)[N], int i) {
+  if constexpr (N == 4) {
+    return i == 0 ? m[0] : (i == 1 ? m[1] : (i == 2 ? m[2] : m[3]));
+  } else {
+    uint32_t r = m[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k) r = i == k ? m[k] : r;
+    return r;
+  }
 }
 
-template <int FMT, int GROUP, bool MX, bool TILED>
+template <int FMT, int GROUP, bool MX, bool TILED, int VPL = kVecPerLane>
 __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
                                                                int64_t ldq, void *__restrict__ scales) {
   constexpr int TPG = GROUP / 8;            // lanes per group
   constexpr int GPS = 32 / TPG;             // groups per slot (2 for 1x128, 8 for MX)
-  constexpr int PAIRS = kVecPerLane * GPS;  // (slot, group) pairs per task: 8 or 32
+  constexpr int PAIRS = VPL * GPS;  // (slot, group) pairs per task: 8 or 32
   static_assert(PAIRS <= 32, "one pair per lane");
+  static_assert(VPL > 0 && (VPL & (VPL - 1)) == 0, "slots per lane: a power of two");
   grid_dependents_launch();  // a GEMM launched after this may set itself up meanwhile
   const int lane = threadIdx.x & 31;
   const int64_t vec_per_row = cols >> 3;
-  const int64_t segs = (vec_per_row + kSegVec - 1) / kSegVec;
+  const int64_t segs = (vec_per_row + (32 * VPL) - 1) / (32 * VPL);
   const int64_t tasks = rows * segs;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
   const float vmax = vmax_of(FMT);
   // the pair this lane computes the scale of
-  const int p_slot = lane % kVecPerLane;
-  const int p_grp = (lane / kVecPerLane) % GPS;
+  const int p_slot = lane % VPL;
+  const int p_grp = (lane / VPL) % GPS;
   for (int64_t t = warp0; t < tasks; t += nwarps) {
     const int64_t r = t / segs;
-    const int64_t cv0 = (t - r * segs) * kSegVec;
-    uint4 v[kVecPerLane];
+    const int64_t cv0 = (t - r * segs) * (32 * VPL);
+    uint4 v[VPL];
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
+    for (int i = 0; i < VPL; ++i) {
       const int64_t cv = cv0 + i * 32 + lane;
       v[i] = cv < vec_per_row ? ld_stream_v4(x + r * ldx + cv * 8) : make_uint4(0, 0, 0, 0);
     }
-    uint32_t m[kVecPerLane];
+    uint32_t m[VPL];
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
+    for (int i = 0; i < VPL; ++i) {
       m[i] = absmax_bits8(v[i]);
 #pragma unroll
       for (int o = TPG / 2; o > 0; o >>= 1) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
     }
     // scale of pair (p_slot, p_grp): every lane of group p_grp holds that group's
     // amax for every slot; lane p_grp * TPG + p_slot offers slot p_slot's value
-    const uint32_t pm = __shfl_sync(0xffffffffu, pick4<0>(m, p_slot), p_grp * TPG + p_slot);
+    const uint32_t pm = __shfl_sync(0xffffffffu, pick(m, p_slot), p_grp * TPG + p_slot);
     const float amax = __uint_as_float(pm << 16);
     const int64_t pcv = cv0 + p_slot * 32 + p_grp * TPG;  // first vector of the pair's group
     float my_inv;
@@ -117,9 +134,9 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
         static_cast<float *>(scales)[(pcv / TPG) * rows + r] = s;
     }
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-      // pair (slot i, this lane's group) was computed by lane group * kVecPerLane + i
-      const float s_inv = __shfl_sync(0xffffffffu, my_inv, (lane / TPG) * kVecPerLane + i);
+    for (int i = 0; i < VPL; ++i) {
+      // pair (slot i, this lane's group) was computed by lane group * VPL + i
+      const float s_inv = __shfl_sync(0xffffffffu, my_inv, (lane / TPG) * VPL + i);
       const int64_t cv = cv0 + i * 32 + lane;
       if (cv >= vec_per_row) continue;
       float f[8];
@@ -453,7 +470,9 @@ __global__ void __launch_bounds__(kChanAmaxThreads, 1) channel_amax_kernel(const
   const int64_t n = active && first < rows ? (rows - 1 - first) / stride + 1 : 0;
   const uint16_t *px = x + first * ldx + v * 8;
   const int64_t step = stride * ldx;
-  auto slot = [&](int st, int i) -> uint4 * { return ring + (st * kChanStageRows + i) * kChanAmaxThreads + threadIdx.x; };
+  auto slot = [&](int st, int i) -> uint4 * {
+    return ring + (st * kChanStageRows + i) * kChanAmaxThreads + threadIdx.x;
+  };
   auto issue = [&](int64_t k0, int st) {
 #pragma unroll
     for (int i = 0; i < kChanStageRows; ++i) {
@@ -532,7 +551,9 @@ __global__ void __launch_bounds__(kChanAmaxThreads, 1) channel_quant_kernel(cons
   const int64_t stride = static_cast<int64_t>(gridDim.y) * g.slabs;
   const int64_t n = active && first < rows ? (rows - 1 - first) / stride + 1 : 0;
   auto row_of = [&](int64_t j) -> int64_t { return first + (n - 1 - j) * stride; };
-  auto slot = [&](int st, int i) -> uint4 * { return ring + (st * kChanStageRows + i) * kChanAmaxThreads + threadIdx.x; };
+  auto slot = [&](int st, int i) -> uint4 * {
+    return ring + (st * kChanStageRows + i) * kChanAmaxThreads + threadIdx.x;
+  };
   auto issue = [&](int64_t j0, int st) {
 #pragma unroll
     for (int i = 0; i < kChanStageRows; ++i) {
@@ -650,9 +671,42 @@ __global__ void __launch_bounds__(kThreads) encode_f32_kernel(const float *__res
   }
 }
 
-int stream_grid(int64_t tasks) {
-  // 8 resident CTAs of 256 threads per SM; never more CTAs than warp tasks need
-  const int64_t full = static_cast<int64_t>(device_sm_count()) * 8;
+// CTAs of `kernel` (256 threads, no dynamic shared memory) resident per SM,
+// looked up once per kernel.
+int resident_per_sm(const void *kernel) {
+  struct Entry {
+    std::atomic<const void *> fn{nullptr};
+    std::atomic<int> occ{0};
+  };
+  static Entry table[48];
+  for (Entry &e : table) {
+    const void *f = e.fn.load(std::memory_order_acquire);
+    if (f == kernel) {
+      const int o = e.occ.load(std::memory_order_acquire);
+      if (o > 0) return o;
+      break;
+    }
+    if (f == nullptr) break;
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess || occ < 1) occ = 1;
+  for (Entry &e : table) {
+    const void *expected = nullptr;
+    if (e.fn.compare_exchange_strong(expected, kernel) || expected == kernel) {
+      e.occ.store(occ, std::memory_order_release);
+      break;
+    }
+  }
+  return occ;
+}
+
+// One wave of the CTAs that can be resident at once (the grid-stride loops
+// assume every warp is running: a second, partial wave of CTAs only lengthens
+// the tail); never more CTAs than warp tasks need.
+template <typename KernelT>
+int stream_grid(KernelT kernel, int64_t tasks) {
+  const int64_t full =
+      static_cast<int64_t>(device_sm_count()) * resident_per_sm(reinterpret_cast<const void *>(kernel));
   const int64_t need = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
   return static_cast<int>(need < full ? (need > 0 ? need : 1) : full);
 }
@@ -665,7 +719,7 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
                              int sf_layout, const float *static_scale, uint8_t *q, int64_t ld_q, void *scales,
                              void *workspace, cudaStream_t stream) {
   const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
-  const int grid = stream_grid(tasks);
+  auto grid_of = [&](auto kernel) { return stream_grid(kernel, tasks); };
   const bool e4 = fmt == FP8_E4M3;
   int launches = 0;
   switch (gran) {
@@ -673,15 +727,15 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
       uint32_t *amax = static_cast<uint32_t *>(workspace);
       if (static_scale == nullptr) {
         if (cudaMemsetAsync(amax, 0, sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
-        amax_kernel<<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, amax);
+        amax_kernel<<<grid_of(amax_kernel), kThreads, 0, stream>>>(x, rows, cols, ld_x, amax);
         ++launches;
       }
       if (e4)
-        quant_tensor_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
-                                                                     static_cast<float *>(scales), amax, static_scale);
+        quant_tensor_kernel<FP8_E4M3><<<grid_of(quant_tensor_kernel<FP8_E4M3>), kThreads, 0, stream>>>(
+            x, rows, cols, ld_x, q, ld_q, static_cast<float *>(scales), amax, static_scale);
       else
-        quant_tensor_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
-                                                                     static_cast<float *>(scales), amax, static_scale);
+        quant_tensor_kernel<FP8_E5M2><<<grid_of(quant_tensor_kernel<FP8_E5M2>), kThreads, 0, stream>>>(
+            x, rows, cols, ld_x, q, ld_q, static_cast<float *>(scales), amax, static_scale);
       ++launches;
       break;
     }
@@ -708,15 +762,20 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
       ++launches;
       break;
     }
-    case FP8_GRAN_TILE_1x128:
+    case FP8_GRAN_TILE_1x128: {
+      const int64_t tile_tasks = rows * ((cols / 8 + 32 * kTileVecPerLane - 1) / (32 * kTileVecPerLane));
+#define FP8BS_TILE(F)                                                                                   \
+  quant_group_kernel<F, 128, false, false, kTileVecPerLane>                                                 \
+      <<<stream_grid(quant_group_kernel<F, 128, false, false, kTileVecPerLane>, tile_tasks), kThreads, 0, \
+         stream>>>(x, rows, cols, ld_x, q, ld_q, scales)
       if (e4)
-        quant_group_kernel<FP8_E4M3, 128, false, false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
-                                                                                     scales);
+        FP8BS_TILE(FP8_E4M3);
       else
-        quant_group_kernel<FP8_E5M2, 128, false, false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q,
-                                                                                     scales);
+        FP8BS_TILE(FP8_E5M2);
+#undef FP8BS_TILE
       ++launches;
       break;
+    }
     case FP8_GRAN_BLOCK_128x128: {
       dim3 g(static_cast<unsigned>(cols / 128), static_cast<unsigned>((rows + 127) / 128));
       if (e4)
@@ -734,8 +793,9 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
         const size_t bytes = static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) * 512;
         if (cudaMemsetAsync(scales, 0, bytes, stream) != cudaSuccess) return FP8_ERR_CUDA;
       }
-#define FP8BS_MX(F, T) \
-  quant_group_kernel<F, 32, true, T><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales)
+#define FP8BS_MX(F, T)                                                                                   \
+  quant_group_kernel<F, 32, true, T><<<grid_of(quant_group_kernel<F, 32, true, T>), kThreads, 0, stream>>>( \
+      x, rows, cols, ld_x, q, ld_q, scales)
       if (e4 && tiled)
         FP8BS_MX(FP8_E4M3, true);
       else if (e4)
@@ -796,25 +856,25 @@ fp8_status_t launch_quantize_delayed(const uint16_t *x, int64_t rows, int64_t co
                                      float *scale_out, cudaStream_t stream) {
   delayed_scale_kernel<<<1, kThreads, 0, stream>>>(history, hlen, slot, margin, fmt, scale_out);
   const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
-  const int grid = stream_grid(tasks);
+  auto grid_of = [&](auto kernel) { return stream_grid(kernel, tasks); };
   uint32_t *rec = reinterpret_cast<uint32_t *>(history + slot);
   if (fmt == FP8_E4M3)
-    quant_tensor_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, nullptr, nullptr,
-                                                                 scale_out, rec);
+    quant_tensor_kernel<FP8_E4M3><<<grid_of(quant_tensor_kernel<FP8_E4M3>), kThreads, 0, stream>>>(
+        x, rows, cols, ld_x, q, ld_q, nullptr, nullptr, scale_out, rec);
   else
-    quant_tensor_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, nullptr, nullptr,
-                                                                 scale_out, rec);
+    quant_tensor_kernel<FP8_E5M2><<<grid_of(quant_tensor_kernel<FP8_E5M2>), kThreads, 0, stream>>>(
+        x, rows, cols, ld_x, q, ld_q, nullptr, nullptr, scale_out, rec);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 fp8_status_t launch_encode_f32(const float *x, int64_t n, int fmt, uint8_t *out, cudaStream_t stream) {
   const int64_t n8 = n / 8;
-  const int grid = stream_grid((n8 + 31) / 32);
+  auto grid_of = [&](auto kernel) { return stream_grid(kernel, (n8 + 31) / 32); };
   if (fmt == FP8_E4M3)
-    encode_f32_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, n8, out);
+    encode_f32_kernel<FP8_E4M3><<<grid_of(encode_f32_kernel<FP8_E4M3>), kThreads, 0, stream>>>(x, n8, out);
   else
-    encode_f32_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, n8, out);
+    encode_f32_kernel<FP8_E5M2><<<grid_of(encode_f32_kernel<FP8_E5M2>), kThreads, 0, stream>>>(x, n8, out);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -823,11 +883,13 @@ fp8_status_t launch_dequantize(const uint8_t *q, int64_t rows, int64_t cols, int
                                int sf_layout, const void *scales, uint16_t *out, int64_t ld_out,
                                cudaStream_t stream) {
   const int64_t tasks = rows * ((cols / 16 + kSegVec - 1) / kSegVec);
-  const int grid = stream_grid(tasks);
+  auto grid_of = [&](auto kernel) { return stream_grid(kernel, tasks); };
   if (fmt == FP8_E4M3)
-    dequant_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
+    dequant_kernel<FP8_E4M3><<<grid_of(dequant_kernel<FP8_E4M3>), kThreads, 0, stream>>>(
+        q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
   else
-    dequant_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
+    dequant_kernel<FP8_E5M2><<<grid_of(dequant_kernel<FP8_E5M2>), kThreads, 0, stream>>>(
+        q, rows, cols, ld_q, gran, sf_layout, scales, out, ld_out);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -884,7 +946,7 @@ static fp8_status_t noalloc_scratch_address(void **out) {
 fp8_status_t launch_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint32_t *amax_bits,
                          cudaStream_t stream) {
   const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
-  amax_kernel<<<stream_grid(tasks), kThreads, 0, stream>>>(x, rows, cols, ld_x, amax_bits);
+  amax_kernel<<<stream_grid(amax_kernel, tasks), kThreads, 0, stream>>>(x, rows, cols, ld_x, amax_bits);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -899,14 +961,14 @@ fp8_status_t launch_quantize_tensor_noalloc(const uint16_t *x, int64_t rows, int
   uint32_t *amax = static_cast<uint32_t *>(scratch);
   if (cudaMemsetAsync(amax, 0, sizeof(uint32_t), stream) != cudaSuccess) return FP8_ERR_CUDA;
   const int64_t tasks = rows * ((cols / 8 + kSegVec - 1) / kSegVec);
-  const int grid = stream_grid(tasks);
-  amax_kernel<<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, amax);
+  auto grid_of = [&](auto kernel) { return stream_grid(kernel, tasks); };
+  amax_kernel<<<grid_of(amax_kernel), kThreads, 0, stream>>>(x, rows, cols, ld_x, amax);
   if (fmt == FP8_E4M3)
-    quant_tensor_kernel<FP8_E4M3><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scale_out, amax,
-                                                                 nullptr);
+    quant_tensor_kernel<FP8_E4M3><<<grid_of(quant_tensor_kernel<FP8_E4M3>), kThreads, 0, stream>>>(
+        x, rows, cols, ld_x, q, ld_q, scale_out, amax, nullptr);
   else
-    quant_tensor_kernel<FP8_E5M2><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scale_out, amax,
-                                                                 nullptr);
+    quant_tensor_kernel<FP8_E5M2><<<grid_of(quant_tensor_kernel<FP8_E5M2>), kThreads, 0, stream>>>(
+        x, rows, cols, ld_x, q, ld_q, scale_out, amax, nullptr);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
