@@ -73,6 +73,10 @@ def load(path: str):
     L.fp8_dequantize_nvfp4.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp]
     L.fp8_gemm_nvfp4.restype = i32
     L.fp8_gemm_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    L.fp8_debug_gemm_mx_pairs.restype = i32
+    L.fp8_debug_gemm_mx_pairs.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
+    L.fp8_debug_gemm_mx_single.restype = i32
+    L.fp8_debug_gemm_mx_single.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
     L.fp8_debug_gemm_blockscaled_pairs.restype = i32
     L.fp8_debug_gemm_blockscaled_pairs.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
     L.fp8_debug_encode_e2m1_f32.restype = i32
@@ -292,6 +296,23 @@ def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, st
     rc = lib().fp8_gemm_mx(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), a_fmt, b_fmt, _ptr(out), M, N, K,
                            _ptr(status), _stream(stream))
     _check(rc, "fp8_gemm_mx")
+    return out
+
+
+def debug_gemm_mx_kernel(kernel: str, a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, status=None,
+                         stream=None):
+    """fp8_gemm_mx on the named kernel: "pairs" (CTA pairs) or "single" (one CTA per tile)."""
+    import torch
+
+    M, K = a.shape
+    N, K2 = b.shape
+    assert K == K2 and a.is_contiguous() and b.is_contiguous() and kernel in ("pairs", "single")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    status = _status(status, a)
+    fn = lib().fp8_debug_gemm_mx_pairs if kernel == "pairs" else lib().fp8_debug_gemm_mx_single
+    rc = fn(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), a_fmt, b_fmt, _ptr(out), M, N, K, _ptr(status), _stream(stream))
+    _check(rc, "fp8_debug_gemm_mx_" + kernel)
     return out
 
 

@@ -308,7 +308,7 @@ fp8_status_t fp8_gemm_blockscaled_quantized_out(const void *a_dev, const float *
 static fp8_status_t gemm_mx_impl(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
                                  const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev,
                                  int64_t M, int64_t N, int64_t K, int *dev_status, fp8_stream_t stream,
-                                 uint64_t wait_ns) {
+                                 uint64_t wait_ns, int mode = 0) {
   fp8_status_t st = check_gemm_common(a_dev, b_dev, out_dev, M, N, K, a_fmt, b_fmt);
   if (st != FP8_OK || M == 0 || N == 0) return st;
   if (K % 32) return FP8_ERR_UNSUPPORTED_SHAPE;
@@ -317,7 +317,7 @@ static fp8_status_t gemm_mx_impl(const void *a_dev, const uint8_t *a_sf_dev, con
   if (dev_status != nullptr && !aligned(dev_status, 4)) return FP8_ERR_ALIGNMENT;
   return launch_gemm_mx(static_cast<const uint8_t *>(a_dev), a_sf_dev, static_cast<const uint8_t *>(b_dev), b_sf_dev,
                         a_fmt, b_fmt, static_cast<uint16_t *>(out_dev), M, N, K, dev_status,
-                        reinterpret_cast<cudaStream_t>(stream), wait_ns);
+                        reinterpret_cast<cudaStream_t>(stream), wait_ns, mode);
 }
 
 fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
@@ -325,6 +325,20 @@ fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void 
                          int *dev_status, fp8_stream_t stream) {
   return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
                       kWaitTimeoutNs);
+}
+
+fp8_status_t fp8_debug_gemm_mx_pairs(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                     const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev,
+                                     int64_t M, int64_t N, int64_t K, int *dev_status, fp8_stream_t stream) {
+  return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
+                      kWaitTimeoutNs, 2);
+}
+
+fp8_status_t fp8_debug_gemm_mx_single(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                      const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev,
+                                      int64_t M, int64_t N, int64_t K, int *dev_status, fp8_stream_t stream) {
+  return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
+                      kWaitTimeoutNs, 1);
 }
 
 fp8_status_t fp8_debug_gemm_blockscaled_wait_limit(const void *a_dev, const float *a_scales_dev, fp8_gran_t a_gran,

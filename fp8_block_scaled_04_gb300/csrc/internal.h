@@ -63,9 +63,10 @@ fp8_status_t launch_gemm_epilogue_scaled(const uint8_t *a, const float *sa, bool
                                          int64_t M, int64_t N, int64_t K, int *dev_status, cudaStream_t stream,
                                          uint64_t wait_ns = kWaitTimeoutNs);
 
+// mode: 0 the shape rule, 1 the single-CTA kernel, 2 the CTA-pair kernel
 fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb, int a_fmt,
                             int b_fmt, uint16_t *out, int64_t M, int64_t N, int64_t K, int *dev_status,
-                            cudaStream_t stream, uint64_t wait_ns = kWaitTimeoutNs);
+                            cudaStream_t stream, uint64_t wait_ns = kWaitTimeoutNs, int mode = 0);
 
 fp8_status_t launch_wait_probe(int *dev_status, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -298,6 +298,21 @@ fp8_status_t fp8_gemm_nvfp4(const void *a_dev, const void *a_sf_dev, const float
 fp8_status_t fp8_debug_encode_f32(const float *x_dev, int64_t n, fp8_format_t fmt, void *out_dev,
                                   fp8_stream_t stream);
 
+/* fp8_gemm_mx on a chosen kernel, whatever the shape rule would pick:
+ * _pairs the CTA-pair kernel (tcgen05 cta_group::2, 256 x 256 tiles over a
+ * cluster of two CTAs, each CTA staging its own halves of the operands),
+ * _single the single-CTA kernel (128 x 256 tiles). Same arguments, layouts and
+ * rules as fp8_gemm_mx ("Low precision: FP8, FP4, and microscaling",
+ * microscaling paragraph); bit-identical results are not promised between
+ * them (the accumulation order inside the tensor core may differ), each is
+ * within the GEMM tolerance. */
+fp8_status_t fp8_debug_gemm_mx_pairs(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                     const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev,
+                                     int64_t M, int64_t N, int64_t K, int *dev_status, fp8_stream_t stream);
+fp8_status_t fp8_debug_gemm_mx_single(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,
+                                      const uint8_t *b_sf_dev, fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev,
+                                      int64_t M, int64_t N, int64_t K, int *dev_status, fp8_stream_t stream);
+
 /* fp8_gemm_blockscaled with 1x128 / 128x128 scales on the CTA-pair kernel
  * (tcgen05 cta_group::2, 256 x 256 tiles over a cluster of two CTAs) whatever
  * the shape: the kernel the library keeps for shapes it may suit but does not

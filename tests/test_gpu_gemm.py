@@ -220,6 +220,27 @@ def test_mx_shapes(M, N, K):
     assert tol.bad == 0, tol
 
 
+@pytest.mark.parametrize("kernel", ["pairs", "single"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (512, 768, 1024), (300, 640, 1024), (130, 272, 416),
+                                   (1, 16, 32), (1024, 1536, 4096), (2304, 512, 640)])
+def test_mx_on_each_kernel(kernel, M, N, K):
+    """Both MXFP8 kernels, whatever the shape rule picks: CTA pairs (256 x 256
+    tiles, each CTA staging its halves of the operands and the scale atoms its
+    tensor core reads) and one CTA per 128 x 256 tile; ragged M, N and K, one
+    pair tile, several tiles per pair."""
+    x = synth.bf16_matrix(M, K, 1.0, 60 + M, 61, 0.005, 50.0)
+    w = synth.bf16_matrix(N, K, 1.0, 62 + N, 63, 0.005, 50.0)
+    qa, sfa, qb, sfb = _quant_pair(x, w, fb.MX32, fb.MX32, layout=fb.SF_TCGEN05)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = fb.debug_gemm_mx_kernel(kernel, *(torch.from_numpy(v).cuda() for v in (qa, sfa, qb, sfb)), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 64)), [M - 1]]))
+    ref, bound = oracle.gemm(qa, sfa, fb.MX32, qb, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05, rows=rows)
+    tol = within_tolerance(out_f64(out)[rows], ref, bound)
+    assert tol.bad == 0, tol
+
+
 def test_mx_unit_scales_equal_plain_path():
     """SF byte 127 (scale 1) everywhere: the block-scaled MMA must equal the plain one."""
     x, w = synth.tiny()
