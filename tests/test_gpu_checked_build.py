@@ -93,6 +93,7 @@ def test_gemms_record_no_stray_store(checked, M, N, K):
     ma, msa = fb.quantize(x, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     mb, msb = fb.quantize(w, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     _eq(*_both(checked, lambda: fb.gemm_mx(ma, msa, mb, msb)))
+    _eq(*_both(checked, lambda: fb.debug_gemm_mx_kernel("pairs", ma, msa, mb, msb)))
     if K % 256 == 0:
         na, nsa, nta = fb.quantize_nvfp4(x)
         nb, nsb, ntb = fb.quantize_nvfp4(w)

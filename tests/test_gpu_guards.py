@@ -94,12 +94,13 @@ def test_mx_and_nvfp4_stay_in_bounds(M, N, K):
     w = synth.bf16_matrix(N, K, 1.0, 1502 + N)
     qa, sfa = oracle.quantize(x, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     qb, sfb = oracle.quantize(w, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
-    out = Guarded((M, N), torch.bfloat16)
-    fb.gemm_mx(*(torch.from_numpy(t).cuda() for t in (qa, sfa, qb, sfb)), out=out.t)
-    assert out.intact()
     ref, bound = oracle.gemm(qa, sfa, fb.MX32, qb, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05)
-    tol = within_tolerance(out_f64(out.t), ref, bound)
-    assert tol.bad == 0, tol
+    for kernel in ("single", "pairs"):
+        out = Guarded((M, N), torch.bfloat16)
+        fb.debug_gemm_mx_kernel(kernel, *(torch.from_numpy(t).cuda() for t in (qa, sfa, qb, sfb)), out=out.t)
+        assert out.intact(), kernel
+        tol = within_tolerance(out_f64(out.t), ref, bound)
+        assert tol.bad == 0, (kernel, tol)
     # NVFP4: codes, padded tiled scale atoms, tensor scale, dequantized output, GEMM output
     xd = to_dev_bf16(x)
     q4 = Guarded((M, K // 2), torch.uint8)
