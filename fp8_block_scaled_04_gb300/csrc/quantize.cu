@@ -35,12 +35,17 @@ constexpr int kThreads = 256;
 constexpr int kVecPerLane = 4;                   // 16-byte vectors in flight per lane
 constexpr int kSegVec = 32 * kVecPerLane;        // vectors a warp covers per task (1024 elements)
 // the 1x128 quantizer keeps eight 16-byte loads in flight per lane (measured
-// +3 % over four; it is latency-bound, and the MX kernels' pair layout allows
-// at most four)
+// +3 % over four: it is latency-bound); the MX-32 quantizer keeps four (eight
+// measured 3 % slower: with 8-element groups its per-group scales then need
+// two rounds of pairs and a gather of every slot's maximum)
 #ifndef FP8BS_TILE_VPL
 #define FP8BS_TILE_VPL 8
 #endif
 constexpr int kTileVecPerLane = FP8BS_TILE_VPL;
+#ifndef FP8BS_MX_VPL
+#define FP8BS_MX_VPL 4
+#endif
+constexpr int kMxVecPerLane = FP8BS_MX_VPL;
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 v;
@@ -80,8 +85,13 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
                                                                int64_t ldq, void *__restrict__ scales) {
   constexpr int TPG = GROUP / 8;            // lanes per group
   constexpr int GPS = 32 / TPG;             // groups per slot (2 for 1x128, 8 for MX)
-  constexpr int PAIRS = VPL * GPS;  // (slot, group) pairs per task: 8 or 32
-  static_assert(PAIRS <= 32, "one pair per lane");
+  constexpr int PAIRS = VPL * GPS;           // (slot, group) pairs per task
+  constexpr int ROUNDS = (PAIRS + 31) / 32;  // pairs per lane
+  // one shuffle fetches a pair's amax when a lane of the pair's group has
+  // the pair's slot index as its own (TPG a multiple of VPL); otherwise the
+  // lane gathers every slot's maximum of the group and picks its slot
+  constexpr bool DIRECT = TPG % VPL == 0;
+  static_assert(ROUNDS <= 2 && (DIRECT || ROUNDS == 2 || PAIRS == 32), "pair layout");
   static_assert(VPL > 0 && (VPL & (VPL - 1)) == 0, "slots per lane: a power of two");
   grid_dependents_launch();  // a GEMM launched after this may set itself up meanwhile
   const int lane = threadIdx.x & 31;
@@ -91,9 +101,6 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
   const float vmax = vmax_of(FMT);
-  // the pair this lane computes the scale of
-  const int p_slot = lane % VPL;
-  const int p_grp = (lane / VPL) % GPS;
   for (int64_t t = warp0; t < tasks; t += nwarps) {
     const int64_t r = t / segs;
     const int64_t cv0 = (t - r * segs) * (32 * VPL);
@@ -110,33 +117,56 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
 #pragma unroll
       for (int o = TPG / 2; o > 0; o >>= 1) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
     }
-    // scale of pair (p_slot, p_grp): every lane of group p_grp holds that group's
-    // amax for every slot; lane p_grp * TPG + p_slot offers slot p_slot's value
-    const uint32_t pm = __shfl_sync(0xffffffffu, pick(m, p_slot), p_grp * TPG + p_slot);
-    const float amax = __uint_as_float(pm << 16);
-    const int64_t pcv = cv0 + p_slot * 32 + p_grp * TPG;  // first vector of the pair's group
-    float my_inv;
-    if (MX) {
-      const int e = mx_shared_exponent(amax, vmax);
-      my_inv = exp2_exact(-e);
-      if (lane < PAIRS && pcv < vec_per_row) {
-        const int64_t j = pcv / TPG;
-        const int64_t ng = cols / 32;
-        uint8_t *sf = static_cast<uint8_t *>(scales);
-        const int64_t si = TILED ? mx_tiled_index(r, j, ng) : r * ng + j;
-        if (FP8BS_GUARD(si, 1, TILED ? ((rows + 127) / 128) * ((ng + 3) / 4) * 512 : rows * ng))
-          sf[si] = static_cast<uint8_t>(e + 127);
+    // lane l computes the scales of pairs l + 32 k (slot = pair % VPL, group =
+    // pair / VPL): every lane of a group holds that group's amax for every slot
+    float my_inv[ROUNDS];
+#pragma unroll
+    for (int k = 0; k < ROUNDS; ++k) {
+      const int pr = lane + 32 * k;
+      const int p_slot = pr % VPL;
+      const int p_grp = (pr / VPL) % GPS;
+      uint32_t pm;
+      if constexpr (DIRECT) {
+        // lane p_grp * TPG + p_slot is in the group and offers slot p_slot's value
+        pm = __shfl_sync(0xffffffffu, pick(m, p_slot), p_grp * TPG + p_slot);
+      } else {
+        pm = 0;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const uint32_t g = __shfl_sync(0xffffffffu, m[i], p_grp * TPG);
+          pm = i == p_slot ? g : pm;
+        }
       }
-    } else {
-      float s;
-      scale_pair(amax, vmax, s, my_inv);
-      if (lane < PAIRS && pcv < vec_per_row && FP8BS_GUARD((pcv / TPG) * rows + r, 1, (cols / GROUP) * rows))
-        static_cast<float *>(scales)[(pcv / TPG) * rows + r] = s;
+      const float amax = __uint_as_float(pm << 16);
+      const int64_t pcv = cv0 + p_slot * 32 + p_grp * TPG;  // first vector of the pair's group
+      if (MX) {
+        const int e = mx_shared_exponent(amax, vmax);
+        my_inv[k] = exp2_exact(-e);
+        if (pr < PAIRS && pcv < vec_per_row) {
+          const int64_t j = pcv / TPG;
+          const int64_t ng = cols / 32;
+          uint8_t *sf = static_cast<uint8_t *>(scales);
+          const int64_t si = TILED ? mx_tiled_index(r, j, ng) : r * ng + j;
+          if (FP8BS_GUARD(si, 1, TILED ? ((rows + 127) / 128) * ((ng + 3) / 4) * 512 : rows * ng))
+            sf[si] = static_cast<uint8_t>(e + 127);
+        }
+      } else {
+        float s;
+        scale_pair(amax, vmax, s, my_inv[k]);
+        if (pr < PAIRS && pcv < vec_per_row && FP8BS_GUARD((pcv / TPG) * rows + r, 1, (cols / GROUP) * rows))
+          static_cast<float *>(scales)[(pcv / TPG) * rows + r] = s;
+      }
     }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      // pair (slot i, this lane's group) was computed by lane group * VPL + i
-      const float s_inv = __shfl_sync(0xffffffffu, my_inv, (lane / TPG) * VPL + i);
+      // pair (slot i, this lane's group) = group * VPL + i, computed in round
+      // pair / 32 by lane pair % 32
+      const int pr = (lane / TPG) * VPL + i;
+      float s_inv = __shfl_sync(0xffffffffu, my_inv[0], pr % 32);
+      if constexpr (ROUNDS > 1) {
+        const float s1 = __shfl_sync(0xffffffffu, my_inv[ROUNDS - 1], pr % 32);
+        s_inv = pr >= 32 ? s1 : s_inv;
+      }
       const int64_t cv = cv0 + i * 32 + lane;
       if (cv >= vec_per_row) continue;
       float f[8];
@@ -789,13 +819,15 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
     }
     case FP8_GRAN_MX32: {
       const bool tiled = sf_layout == FP8_SF_TCGEN05;
+      const int64_t mx_tasks = rows * ((cols / 8 + 32 * kMxVecPerLane - 1) / (32 * kMxVecPerLane));
       if (tiled && (rows % 128 != 0 || cols % 128 != 0)) {
         const size_t bytes = static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) * 512;
         if (cudaMemsetAsync(scales, 0, bytes, stream) != cudaSuccess) return FP8_ERR_CUDA;
       }
-#define FP8BS_MX(F, T)                                                                                   \
-  quant_group_kernel<F, 32, true, T><<<grid_of(quant_group_kernel<F, 32, true, T>), kThreads, 0, stream>>>( \
-      x, rows, cols, ld_x, q, ld_q, scales)
+#define FP8BS_MX(F, T)                                                                              \
+  quant_group_kernel<F, 32, true, T, kMxVecPerLane>                                                    \
+      <<<stream_grid(quant_group_kernel<F, 32, true, T, kMxVecPerLane>, mx_tasks), kThreads, 0, stream>>>( \
+          x, rows, cols, ld_x, q, ld_q, scales)
       if (e4 && tiled)
         FP8BS_MX(FP8_E4M3, true);
       else if (e4)
