@@ -316,7 +316,7 @@ fp8_status_t fp8_debug_gemm_mx_single(const void *a_dev, const uint8_t *a_sf_dev
 /* fp8_gemm_blockscaled with 1x128 / 128x128 scales on the CTA-pair kernel
  * (tcgen05 cta_group::2, 256 x 256 tiles over a cluster of two CTAs) whatever
  * the shape: the kernel the library keeps for shapes it may suit but does not
- * select by default (it measured 3-5 % slower than the single-CTA kernel on the
+ * select by default (it measured 2 % slower than the single-CTA kernel on the
  * prefill shapes). Same arguments and rules as fp8_gemm_blockscaled with
  * a_gran = TILE_1x128, b_gran = BLOCK_128x128. */
 fp8_status_t fp8_debug_gemm_blockscaled_pairs(const void *a_dev, const float *a_scales_dev, const void *b_dev,
