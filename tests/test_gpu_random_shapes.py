@@ -89,3 +89,34 @@ def test_nvfp4_gemm_random_shapes(M, N, K):
     ref, bound = oracle.gemm_nvfp4(qa, sfa, ta, qb, sfb, tb, rows=rows, cols=cols)
     tol = within_tolerance(out_f64(out)[np.ix_(rows, cols)], ref, bound)
     assert tol.bad == 0, tol
+
+
+_GRAN_UNITS = [(fb.TENSOR, fb.SF_LINEAR, 16), (fb.TOKEN, fb.SF_LINEAR, 16), (fb.CHANNEL, fb.SF_LINEAR, 16),
+               (fb.TILE_1x128, fb.SF_LINEAR, 128), (fb.BLOCK_128x128, fb.SF_LINEAR, 128),
+               (fb.MX32, fb.SF_LINEAR, 32), (fb.MX32, fb.SF_TCGEN05, 32)]
+
+
+def _quant_cases(seed, n):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        gran, lay, unit = _GRAN_UNITS[i % len(_GRAN_UNITS)]
+        rows = int(rng.choice([rng.integers(1, 130), rng.integers(130, 5000)]))
+        cols = unit * int(rng.integers(1, max(2, 20000 // unit)))
+        fmt = fb.E4M3 if rng.integers(0, 2) == 0 else fb.E5M2
+        cases.append((gran, lay, fmt, rows, cols))
+    return cases
+
+
+@pytest.mark.parametrize("gran,lay,fmt,rows,cols", _quant_cases(2027, 28))
+def test_quantize_random_shapes_bit_exact(gran, lay, fmt, rows, cols):
+    """Every granularity and scale layout on seeded random shapes (ragged row and column
+    tails, one row, many rows): codes and scales bit-exact, dequantized values too."""
+    x = synth.bf16_matrix(rows, cols, 1.0, 930 + rows, 931 + cols, 0.01, 40.0)
+    q, s = fb.quantize(to_dev_bf16(x), fmt, gran, lay)
+    oq, os_ = oracle.quantize(x, fmt, gran, lay)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint8).reshape(-1), np.ascontiguousarray(os_).view(np.uint8).reshape(-1))
+    d = fb.dequantize(q, s, fmt, gran, lay)
+    ref = oracle.dequantize(oq, os_, fmt, gran, lay)
+    assert np.array_equal(d.view(torch.int16).cpu().numpy().view(np.uint16), ref)
