@@ -817,7 +817,8 @@ struct SwapCfg {
   static constexpr int BXW = BX / G;                   // activation rows per fold warp
   static constexpr int FOLD_WARPS = 4 * G;
   static constexpr int ISSUERS = SWAP_MMA_ISSUERS;      // MMA-issuing warps 1 .. ISSUERS
-  static constexpr int FIRST_FOLD_WARP = 1 + ISSUERS;
+  static constexpr int SCALE_WARP = 1 + ISSUERS;       // copies the scale chunks (tensor-copy path)
+  static constexpr int FIRST_FOLD_WARP = 2 + ISSUERS;
   static constexpr int THREADS = 32 * (FIRST_FOLD_WARP + FOLD_WARPS);
   static_assert(ISSUERS >= 1 && ISSUERS <= 2 && NBUF % ISSUERS == 0, "each partial buffer needs one issuer");
   static constexpr uint32_t TMEM_COLS = NBUF * BX <= 32 ? 32 : (NBUF * BX <= 64 ? 64 : (NBUF * BX <= 128 ? 128 : 256));
@@ -902,47 +903,46 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   const uint32_t tmem = ctl.tmem_base;
   float *scbuf = reinterpret_cast<float *>(smem + C::SC_OFFSET);
 
-  if (warp == 0) {
-    if (lane == 0) {
-      int it = 0, chunk = 0;
+  if (warp == C::SCALE_WARP) {
+    // scale chunks (tensor-copy path): KBC k-blocks of s_x[kb, tile rows] and
+    // s_w[tile, kb] per chunk into the next of two slots, each as soon as the
+    // fold warps have read the chunk that held the slot (boxes past K or M read
+    // as zeros); a thread of its own, so that the weight stream never waits
+    // behind these copies
+    if (lane == 0 && sc_tma) {
+      int chunk = 0;
       bool ok = true;
-      // scale chunk: KBC k-blocks of tile t from k-block kb0 into the next slot
-      // (boxes past K or M read as zeros)
-      auto issue_chunk = [&](int t, int kb0) -> bool {
-        const int slot = chunk & 1;
-        if (!mbar_wait(&sempty[slot], ((chunk >> 1) & 1) ^ 1, wait_ns, &ctl.abort)) return false;
-        const int wt = t / num_x, xt = t - wt * num_x;
-        float *dst = scbuf + slot * (C::SC_SLOT_BYTES / 4);
-        mbar_arrive_expect_tx(&sfull[slot], C::SC_TX_BYTES);
-        tma_load_2d(dst, &tmSX, xt * BX, kb0, &sfull[slot]);
-        tma_load_2d(dst + C::SC_W_OFF, &tmSW, kb0, wt, &sfull[slot]);
-        ++chunk;
-        return true;
-      };
-      if (sc_tma && static_cast<int>(blockIdx.x) < ntiles) ok = issue_chunk(blockIdx.x, 0);
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int wt = tile / num_x, xt = tile - wt * num_x;
+        for (int kb0 = 0; kb0 < KB; kb0 += C::KBC) {
+          const int slot = chunk & 1;
+          if (!mbar_wait(&sempty[slot], ((chunk >> 1) & 1) ^ 1, wait_ns, &ctl.abort)) {
+            ok = false;
+            break;
+          }
+          float *dst = scbuf + slot * (C::SC_SLOT_BYTES / 4);
+          mbar_arrive_expect_tx(&sfull[slot], C::SC_TX_BYTES);
+          tma_load_2d(dst, &tmSX, xt * BX, kb0, &sfull[slot]);
+          tma_load_2d(dst + C::SC_W_OFF, &tmSW, kb0, wt, &sfull[slot]);
+          ++chunk;
+        }
+      }
+      if (!ok) {
+        flag_abort(&ctl, dev_status);
+        // the last two chunks' copies may still be in flight (an earlier one
+        // has been waited for by the fold warps before its slot was reused)
+        for (int c = chunk > 2 ? chunk - 2 : 0; c < chunk; ++c)
+          mbar_wait(&sfull[c & 1], (c >> 1) & 1, kDrainTimeoutNs, nullptr);
+      }
+    }
+  } else if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int wt = tile / num_x, xt = tile - wt * num_x;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
-          if (sc_tma) {
-            // the next chunk's copies start halfway through this one: their
-            // slot held the chunk before this one, which the fold warps (at
-            // most STAGES k-blocks behind) have finished by then, and the
-            // copies have half a chunk of k-blocks to land
-            const int c0 = kb - kb % C::KBC;
-            const int clen = min(C::KBC, KB - c0);
-            if (kb == c0 + min(C::KBC / 2, clen - 1)) {
-              int t_next = tile, kb_next = c0 + C::KBC;
-              if (kb_next >= KB) {
-                t_next = tile + static_cast<int>(gridDim.x);
-                kb_next = 0;
-              }
-              if (t_next < ntiles && !issue_chunk(t_next, kb_next)) {
-                ok = false;
-                break;
-              }
-            }
-          }
           if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, wait_ns, &ctl.abort)) {
             ok = false;
             break;
@@ -956,13 +956,9 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       if (!ok) {
         flag_abort(&ctl, dev_status);
         drain_stages<STAGES>(full, it);
-        // the last two chunks' copies may still be in flight (an earlier one
-        // has been waited for by the fold warps before its slot was reused)
-        for (int c = chunk > 2 ? chunk - 2 : 0; c < chunk; ++c)
-          mbar_wait(&sfull[c & 1], (c >> 1) & 1, kDrainTimeoutNs, nullptr);
       }
     }
-  } else if (warp < C::FIRST_FOLD_WARP) {
+  } else if (warp <= C::ISSUERS) {
     // MMA issuers: issuer j takes the k-blocks with kc % ISSUERS == j (so each
     // partial buffer is written by one thread and its MMAs stay in order);
     // one thread's waits, MMAs and commit take about a k-block's worth of HBM
