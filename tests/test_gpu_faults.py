@@ -131,3 +131,32 @@ def test_default_status_word_reports_timeouts():
         fb.check_status()
     assert e.value.code == fb.ERR_TIMEOUT
     fb.check_status()  # cleared
+
+
+def test_empty_gemms_launch_nothing_and_k0_is_refused():
+    """M = 0 or N = 0 is an empty product: every GEMM entry returns OK and launches
+    nothing. K = 0 with M, N > 0 has no scale blocks to fold: refused as a shape."""
+    d = "cuda"
+    u8 = lambda *s: torch.zeros(s, dtype=torch.uint8, device=d)  # noqa: E731
+    f32 = lambda n: torch.ones(n, dtype=torch.float32, device=d)  # noqa: E731
+    n0 = fb.launch_count()
+    for M, N in ((0, 256), (128, 0), (0, 0)):
+        K = 256
+        a, b = u8(M, K), u8(N, K)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+        fb.gemm_blockscaled(a, f32(max(1, M * 2)), fb.TILE_1x128, b, f32(max(1, N)), fb.BLOCK_128x128, out=out)
+        fb.gemm_blockscaled(a, f32(1), fb.TENSOR, b, f32(1), fb.TENSOR, out=out)
+        fb.gemm_mx(a, u8(4096), b, u8(4096), out=out)
+        fb.gemm_nvfp4(u8(M, K // 2), u8(4096), f32(1), u8(N, K // 2), u8(4096), f32(1), out=out)
+        if N % 128 == 0:
+            fb.gemm_blockscaled_quantized_out(a, f32(max(1, M * 2)), b, f32(max(1, N)))
+    torch.cuda.synchronize()
+    assert fb.launch_count() == n0
+    a, b = u8(16, 0), u8(128, 0)
+    for call in (lambda: fb.gemm_blockscaled(a, f32(1), fb.TILE_1x128, b, f32(1), fb.BLOCK_128x128),
+                 lambda: fb.gemm_blockscaled(a, f32(1), fb.TENSOR, b, f32(1), fb.TENSOR),
+                 lambda: fb.gemm_mx(a, u8(512), b, u8(512))):
+        with pytest.raises(fb.Fp8Error) as e:
+            call()
+        assert e.value.code == fb.ERR_UNSUPPORTED_SHAPE
+    assert fb.launch_count() == n0
