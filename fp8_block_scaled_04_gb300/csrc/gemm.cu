@@ -806,7 +806,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FoldPairCfg<STAGES>:
 // activation rows (G groups of four fold warps, BXW = SWAP_FOLD_COLS: with
 // all 64 rows per warp the fold warps, not HBM, set the k-block rate); the
 // activation scales s_x[kb, m] vary along its row and reach every lane as
-// shared-memory broadcasts. Two threads issue the MMAs, alternate k-blocks.
+// shared-memory broadcasts. Two threads issue the MMAs, alternate k-blocks;
+// a warp of its own copies the scale chunks, so that the W stream never waits
+// for a chunk slot.
 template <int BX, int STAGES>
 struct SwapCfg {
   static constexpr int W_BYTES = BM * BK;
@@ -1013,9 +1015,9 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
       const float *sb_blk = sb + static_cast<int64_t>(wt) * KB;  // one 128-row weight block per tile
 #pragma unroll
       for (int j = 0; j < BXW / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-      // Scales, tensor-copy path (sc_tma): the producer brings s_x and s_w of
-      // KBC k-blocks at a time into a chunk slot; every lane reads them back
-      // as shared-memory broadcasts and forms s_w * s_x itself.
+      // Scales, tensor-copy path (sc_tma): the scale warp brings s_x and s_w
+      // of KBC k-blocks at a time into a chunk slot; every lane reads them
+      // back as shared-memory broadcasts and forms s_w * s_x itself.
       // Register path (a layout the tensor copies cannot describe): lane l
       // holds s_x[kb, m0 + 32 r + l] and s_w[kb] in one of two fixed register
       // slots (even / odd k-blocks), loaded two k-blocks ahead and reloaded in
