@@ -829,6 +829,7 @@ struct SwapCfg {
   // scale chunks (when the scales' layout allows tensor copies): two slots,
   // each KBC k-blocks of s_x[kb, tile's BX rows] followed by s_w[tile, kb]
   static constexpr int KBC = BX >= 64 ? 28 : 64;
+  static constexpr int SC_HEAD = 4;  // k-blocks of a chunk whose products come first
   static constexpr int SC_X_BYTES = KBC * BX * 4;
   static constexpr int SC_W_OFF = SC_X_BYTES / 4;                  // in floats
   static constexpr int SC_SLOT_BYTES = SC_X_BYTES + ((KBC * 4 + 127) / 128) * 128;
@@ -836,6 +837,7 @@ struct SwapCfg {
   static constexpr int SC_OFFSET = STAGES * STAGE_BYTES + CBUF_BYTES + OTILE_BYTES;
   static constexpr int SMEM = SC_OFFSET + 2 * SC_SLOT_BYTES + 1024;
   static_assert(KBC % 4 == 0 && KBC <= 256 && SC_X_BYTES % 128 == 0 && SC_OFFSET % 128 == 0, "scale chunk layout");
+  static_assert(SC_HEAD > 0 && SC_HEAD < KBC && (SC_HEAD * BX) % 32 == 0, "head of a chunk");
   static_assert(BX % 16 == 0 && BX <= 64, "MMA N side");
   static_assert(SMEM + 256 <= 232448, "shared memory budget");
 };
@@ -854,8 +856,10 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
   // stage's next k-block needs the release of k-block kc + NBUF first, and
   // STAGES > NBUF)
   static_assert(STAGES > C::NBUF, "stage barrier parity");
-  // sfull / sempty: the two scale-chunk slots (landed / read by every fold warp)
-  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[C::NBUF], drain, sfull[2], sempty[2];
+  // sfull / phead / pready / sempty: the two scale-chunk slots (landed /
+  // products of the first SC_HEAD k-blocks formed by the scale warp / all its
+  // products formed / read by every fold warp)
+  __shared__ uint64_t full[STAGES], empty[STAGES], tempty[C::NBUF], drain, sfull[2], phead[2], pready[2], sempty[2];
   __shared__ SharedCtl ctl;
 
   const int warp = threadIdx.x >> 5;
@@ -874,6 +878,8 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
     mbar_init(&drain, C::ISSUERS);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&sfull[j], 1);
+      mbar_init(&phead[j], 1);
+      mbar_init(&pready[j], 1);
       mbar_init(&sempty[j], C::FOLD_WARPS);
     }
     ctl.abort = 0;
@@ -909,30 +915,50 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
     // scale chunks (tensor-copy path): KBC k-blocks of s_x[kb, tile rows] and
     // s_w[tile, kb] per chunk into the next of two slots, each as soon as the
     // fold warps have read the chunk that held the slot (boxes past K or M read
-    // as zeros); a thread of its own, so that the weight stream never waits
-    // behind these copies
-    if (lane == 0 && sc_tma) {
+    // as zeros); once a chunk has landed the warp turns each s_x in place into
+    // the product s_w[kb] * s_x[kb, m] the fold applies (formed once here
+    // instead of in every fold warp of the four lane quarters). A warp of its
+    // own, so that the weight stream never waits behind these copies.
+    if (sc_tma) {
       int chunk = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int wt = tile / num_x, xt = tile - wt * num_x;
         for (int kb0 = 0; kb0 < KB; kb0 += C::KBC) {
           const int slot = chunk & 1;
-          if (!mbar_wait(&sempty[slot], ((chunk >> 1) & 1) ^ 1, wait_ns, &ctl.abort)) {
+          const bool free_slot = mbar_wait(&sempty[slot], ((chunk >> 1) & 1) ^ 1, wait_ns, &ctl.abort);
+          if (!__all_sync(0xffffffffu, free_slot)) {
             ok = false;
             break;
           }
           float *dst = scbuf + slot * (C::SC_SLOT_BYTES / 4);
-          mbar_arrive_expect_tx(&sfull[slot], C::SC_TX_BYTES);
-          tma_load_2d(dst, &tmSX, xt * BX, kb0, &sfull[slot]);
-          tma_load_2d(dst + C::SC_W_OFF, &tmSW, kb0, wt, &sfull[slot]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sfull[slot], C::SC_TX_BYTES);
+            tma_load_2d(dst, &tmSX, xt * BX, kb0, &sfull[slot]);
+            tma_load_2d(dst + C::SC_W_OFF, &tmSW, kb0, wt, &sfull[slot]);
+          }
           ++chunk;
+          const bool landed = mbar_wait(&sfull[slot], ((chunk - 1) >> 1) & 1, wait_ns, &ctl.abort);
+          if (!__all_sync(0xffffffffu, landed)) {
+            ok = false;
+            break;
+          }
+          // the first SC_HEAD k-blocks first, so that the fold warps can start
+          // the chunk while the rest are formed
+#pragma unroll
+          for (int i = lane; i < C::SC_HEAD * BX; i += 32) dst[i] = dst[C::SC_W_OFF + i / BX] * dst[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&phead[slot]);
+#pragma unroll 4
+          for (int i = C::SC_HEAD * BX + lane; i < C::KBC * BX; i += 32) dst[i] = dst[C::SC_W_OFF + i / BX] * dst[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pready[slot]);
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         flag_abort(&ctl, dev_status);
         // the last two chunks' copies may still be in flight (an earlier one
-        // has been waited for by the fold warps before its slot was reused)
+        // has been waited for before its slot was reused)
         for (int c = chunk > 2 ? chunk - 2 : 0; c < chunk; ++c)
           mbar_wait(&sfull[c & 1], (c >> 1) & 1, kDrainTimeoutNs, nullptr);
       }
@@ -1016,8 +1042,9 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
 #pragma unroll
       for (int j = 0; j < BXW / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       // Scales, tensor-copy path (sc_tma): the scale warp brings s_x and s_w
-      // of KBC k-blocks at a time into a chunk slot; every lane reads them
-      // back as shared-memory broadcasts and forms s_w * s_x itself.
+      // of KBC k-blocks at a time into a chunk slot and forms the products
+      // s_w * s_x there; every lane reads them back as shared-memory
+      // broadcasts.
       // Register path (a layout the tensor copies cannot describe): lane l
       // holds s_x[kb, m0 + 32 r + l] and s_w[kb] in one of two fixed register
       // slots (even / odd k-blocks), loaded two k-blocks ahead and reloaded in
@@ -1042,9 +1069,10 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         const int kl = kb % C::KBC;
         const float *sxc = scbuf + (chunk & 1) * (C::SC_SLOT_BYTES / 4);
         if (sc_tma) {
-          if (kl == 0) {
-            const bool landed = mbar_wait(&sfull[chunk & 1], (chunk >> 1) & 1, wait_ns, &ctl.abort);
-            if (!__all_sync(0xffffffffu, landed)) return false;
+          if (kl == 0 || kl == C::SC_HEAD) {
+            const bool ready =
+                mbar_wait(kl == 0 ? &phead[chunk & 1] : &pready[chunk & 1], (chunk >> 1) & 1, wait_ns, &ctl.abort);
+            if (!__all_sync(0xffffffffu, ready)) return false;
           }
         } else {
           // the slot is rewritten two k-blocks later, after the __syncwarp
@@ -1069,15 +1097,14 @@ __global__ void __launch_bounds__(SwapCfg<BX, STAGES>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
         if (sc_tma) {
-          const float w = sxc[C::SC_W_OFF + kl];
-          const float2 w2 = make_float2(w, w);
-          const float4 *x4 = reinterpret_cast<const float4 *>(sxc + kl * BX + col0);
+          // the products s_w * s_x of this k-block's rows col0 .. col0 + BXW - 1
+          const float4 *c4 = reinterpret_cast<const float4 *>(sxc + kl * BX + col0);
 #pragma unroll
           for (int i = 0; i < BXW / 4; ++i) {
-            const float4 xv = x4[i];
-            acc[2 * i] = __ffma2_rn(__fmul2_rn(w2, make_float2(xv.x, xv.y)),
+            const float4 c = c4[i];
+            acc[2 * i] = __ffma2_rn(make_float2(c.x, c.y),
                                     make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), acc[2 * i]);
-            acc[2 * i + 1] = __ffma2_rn(__fmul2_rn(w2, make_float2(xv.z, xv.w)),
+            acc[2 * i + 1] = __ffma2_rn(make_float2(c.z, c.w),
                                         make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])),
                                         acc[2 * i + 1]);
           }
