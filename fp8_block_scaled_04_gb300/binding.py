@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "fp8bs.h")
 
 E4M3, E5M2 = 0, 1
 TENSOR, TOKEN, TILE_1x128, BLOCK_128x128, MX32, CHANNEL = 0, 1, 2, 3, 4, 5
-SF_LINEAR, SF_TCGEN05 = 0, 1
+SF_LINEAR, SF_TCGEN05, SF_TCGEN05_X4 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 
 _lib = None
@@ -65,6 +65,8 @@ def load(path: str):
     L.fp8_gemm_blockscaled_quantized_out.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, vp, vp]
     L.fp8_gemm_mx.restype = i32
     L.fp8_gemm_mx.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
+    L.fp8_gemm_mx_x4.restype = i32
+    L.fp8_gemm_mx_x4.argtypes = [vp, vp, vp, vp, i32, i32, vp, i64, i64, i64, vp, vp]
     L.fp8_nvfp4_scales_bytes.restype = sz
     L.fp8_nvfp4_scales_bytes.argtypes = [i64, i64, i32]
     L.fp8_quantize_nvfp4.restype = i32
@@ -283,19 +285,23 @@ def gemm_blockscaled_quantized_out(a, a_scales, b, b_scales, a_fmt: int = E4M3, 
     return q_out, q_scales
 
 
-def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, status=None, stream=None):
-    """MXFP8 GEMM; a_sf / b_sf in the SF_TCGEN05 layout."""
+def gemm_mx(a, a_sf, b, b_sf, a_fmt: int = E4M3, b_fmt: int = E4M3, out=None, status=None, stream=None,
+            sf_layout: int = SF_TCGEN05):
+    """MXFP8 GEMM; a_sf / b_sf in the SF_TCGEN05 layout (fp8_gemm_mx) or, with
+    sf_layout=SF_TCGEN05_X4, in the staged-four-times layout (fp8_gemm_mx_x4)."""
     import torch
 
     M, K = a.shape
     N, K2 = b.shape
     assert K == K2 and a.is_contiguous() and b.is_contiguous()
+    assert sf_layout in (SF_TCGEN05, SF_TCGEN05_X4)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     status = _status(status, a)
-    rc = lib().fp8_gemm_mx(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), a_fmt, b_fmt, _ptr(out), M, N, K,
-                           _ptr(status), _stream(stream))
-    _check(rc, "fp8_gemm_mx")
+    fn = lib().fp8_gemm_mx if sf_layout == SF_TCGEN05 else lib().fp8_gemm_mx_x4
+    rc = fn(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), a_fmt, b_fmt, _ptr(out), M, N, K, _ptr(status),
+            _stream(stream))
+    _check(rc, "fp8_gemm_mx" if sf_layout == SF_TCGEN05 else "fp8_gemm_mx_x4")
     return out
 
 

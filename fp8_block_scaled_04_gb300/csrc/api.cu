@@ -133,8 +133,9 @@ size_t fp8_scales_bytes(int64_t rows, int64_t cols, fp8_gran_t gran, fp8_sf_layo
       return cols % 128 ? 0 : static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>(cols / 128) * sizeof(float);
     case FP8_GRAN_MX32:
       if (cols % 32) return 0;
-      if (sf_layout == FP8_SF_TCGEN05)
-        return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) * 512;
+      if (sf_layout == FP8_SF_TCGEN05 || sf_layout == FP8_SF_TCGEN05_X4)
+        return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) *
+               (sf_layout == FP8_SF_TCGEN05 ? 512 : 2048);
       if (sf_layout == FP8_SF_LINEAR) return static_cast<size_t>(rows) * static_cast<size_t>(cols / 32);
       return 0;
     default: return 0;
@@ -167,7 +168,8 @@ fp8_status_t fp8_quantize(const void *x_dev, int64_t rows, int64_t cols, int64_t
                           int64_t ld_q, void *scales_dev, void *workspace_dev, size_t workspace_bytes,
                           fp8_stream_t stream) {
   if (!valid_fmt(fmt) || !valid_gran(gran)) return FP8_ERR_INVALID_ARG;
-  if (sf_layout != FP8_SF_LINEAR && !(gran == FP8_GRAN_MX32 && sf_layout == FP8_SF_TCGEN05))
+  if (sf_layout != FP8_SF_LINEAR &&
+      !(gran == FP8_GRAN_MX32 && (sf_layout == FP8_SF_TCGEN05 || sf_layout == FP8_SF_TCGEN05_X4)))
     return FP8_ERR_INVALID_ARG;
   if (static_scale_dev != nullptr && gran != FP8_GRAN_TENSOR) return FP8_ERR_INVALID_ARG;
   fp8_status_t st = check_quant_shape(rows, cols, gran);
@@ -227,7 +229,8 @@ fp8_status_t fp8_dequantize(const void *q_dev, int64_t rows, int64_t cols, int64
                             fp8_gran_t gran, fp8_sf_layout_t sf_layout, const void *scales_dev, void *out_dev,
                             int64_t ld_out, fp8_stream_t stream) {
   if (!valid_fmt(fmt) || !valid_gran(gran)) return FP8_ERR_INVALID_ARG;
-  if (sf_layout != FP8_SF_LINEAR && !(gran == FP8_GRAN_MX32 && sf_layout == FP8_SF_TCGEN05))
+  if (sf_layout != FP8_SF_LINEAR &&
+      !(gran == FP8_GRAN_MX32 && (sf_layout == FP8_SF_TCGEN05 || sf_layout == FP8_SF_TCGEN05_X4)))
     return FP8_ERR_INVALID_ARG;
   fp8_status_t st = check_quant_shape(rows, cols, gran);
   if (st != FP8_OK) return st;
@@ -325,6 +328,13 @@ fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void 
                          int *dev_status, fp8_stream_t stream) {
   return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
                       kWaitTimeoutNs);
+}
+
+fp8_status_t fp8_gemm_mx_x4(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
+                            fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
+                            int *dev_status, fp8_stream_t stream) {
+  return gemm_mx_impl(a_dev, a_sf_dev, b_dev, b_sf_dev, a_fmt, b_fmt, out_dev, M, N, K, dev_status, stream,
+                      kWaitTimeoutNs, 3);
 }
 
 fp8_status_t fp8_debug_gemm_mx_pairs(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev,

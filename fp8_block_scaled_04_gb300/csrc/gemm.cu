@@ -39,6 +39,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "internal.h"
 #include "fp8_math.cuh"
@@ -1437,7 +1438,9 @@ __global__ void __launch_bounds__(SwapSplitCfg<BX, STAGES>::THREADS, 1)
 // MXFP8 (KIND_MX8: UE8M0 scale per 32 K) or NVFP4 (KIND_NVF4: E2M1 operands,
 // E4M3 scale per 16 K, fp32 tensor scales applied in the epilogue)
 // =====================================================================
-constexpr int KIND_EPI = 0, KIND_MX8 = 1, KIND_NVF4 = 2;
+// KIND_MX8W: MXFP8 with both operands' scales in the staged-four-times
+// layout (each 512-byte atom stored four times in a row, 2048 bytes).
+constexpr int KIND_EPI = 0, KIND_MX8 = 1, KIND_NVF4 = 2, KIND_MX8W = 3;
 
 // A stage always holds 128 bytes of K per row: 128 fp8 or 256 fp4 elements.
 // Scale atoms (128 rows x 4 scales, 512 bytes) per stage and 128-row block:
@@ -1446,10 +1449,20 @@ template <int KIND, int BN, int STAGES, int NACC>
 struct AccCfg {
   static constexpr bool MX = KIND != KIND_EPI;
   static constexpr int ATOMS = KIND == KIND_NVF4 ? 4 : (MX ? 1 : 0);
+  // KIND_MX8W: a stage's atoms reach tensor memory in two copies instead of
+  // three. Each tcgen05.cp costs tensor-pipe time whatever its size, and the
+  // 128-lane copy shapes put row r of their source in lane r, so an atom
+  // staged four times over (row r = atom row r % 32: what .32x128b.warpx4
+  // replicates to the four lane quarters) lets one .128x256b copy take both
+  // W atoms (2048 bytes apart) and one .128x128b copy X's; tensor memory ends
+  // up the same, byte for byte.
+  static constexpr bool WIDE = KIND == KIND_MX8W;
+  static constexpr int ATOM_BYTES = WIDE ? 2048 : 512;  // one atom as staged
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
-  static constexpr int SFA_BYTES = 512 * ATOMS;
-  static constexpr int SFB_BYTES = 512 * ATOMS * (BN / 128);
+  static constexpr int SFA_BYTES = ATOM_BYTES * ATOMS;
+  static constexpr int SFB_BYTES = ATOM_BYTES * ATOMS * (BN / 128);
+  static_assert(!WIDE || BN == 256, "the wide copy takes two 128-row W atoms");
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_STRIDE = (STAGE_BYTES + 1023) / 1024 * 1024;
   static constexpr int CONSUMER_WARPS = 4 * (BN / 128);
@@ -1469,11 +1482,14 @@ struct AccCfg {
   // full.
   static constexpr bool SF_SPLIT = COPIER && KIND == KIND_NVF4;
   static constexpr int THREADS = 32 * FIRST_CONSUMER_WARP + 32 * CONSUMER_WARPS;
-  static constexpr int SF_COLS = 4 * ATOMS * (1 + BN / 128);  // tensor-memory columns per stage
+  // tensor-memory columns per stage (WIDE: 12 used, 16 so that each stage's
+  // columns start 16-aligned)
+  static constexpr int SF_COLS = WIDE ? 16 : 4 * ATOMS * (1 + BN / 128);
   static constexpr int ACC_COLS = NACC * BN;                    // NACC accumulators (2: epilogue overlaps MMA)
   static constexpr uint32_t TMEM_COLS = ACC_COLS + STAGES * SF_COLS <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_STRIDE + 1024;
   static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory budget");
+  static_assert(!WIDE || !COPIER, "the MMA thread copies the staged atoms itself");
 };
 
 // A stage's scale atoms, shared memory (A's atoms, then B's per 128-row block;
@@ -1578,7 +1594,7 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
           // early; otherwise they follow the operands on the stage's barrier
           // (operands first measured 2.6 % faster there).
           auto load_atoms = [&](uint64_t *bar) {
-            constexpr int AB = 512 * C::ATOMS;
+            constexpr int AB = C::ATOM_BYTES * C::ATOMS;
             bulk_load(st + C::A_BYTES + C::B_BYTES, sfa + (static_cast<int64_t>(mt) * KB + kb) * AB, AB, bar);
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j) {
@@ -1661,9 +1677,17 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          if constexpr (MX && !C::COPIER)
+          if constexpr (C::WIDE) {
+            // X's staged atom at +0 -> columns +8..11; W's two at +2048 and
+            // +4096 (16-byte column chunks 0 and 1 of one source) -> +0..7
+            const uint32_t sft = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
+            const uint32_t sf0 = b0 + C::B_BYTES;
+            tmem_cp_128x256b(sft, sdesc_plain(sf0 + C::SFA_BYTES, C::ATOM_BYTES, 128));
+            tmem_cp_128x128b(sft + 8, sdesc_plain(sf0, 128, 128));
+          } else if constexpr (MX && !C::COPIER) {
             copy_scale_atoms<KIND, BN>(tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS),
                                        sdesc_plain_32x16(b0 + C::B_BYTES));
+          }
           if (F4) {
             // NVFP4: one scale atom per MMA (K = 64, four 16-element scales per
             // row); A's atom k at column +4k, B's at +8k (second 128-row block
@@ -1675,8 +1699,11 @@ __global__ void __launch_bounds__(AccCfg<KIND, BN, STAGES, NACC>::THREADS, 1)
               mma_mxf4nvf4(d, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_t + 4 * k,
                            sfb_t + 8 * k, (kb > 0 || k > 0) ? 1u : 0u);
           } else if (MX) {
-            const uint32_t sfa_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
-            const uint32_t sfb_t = sfa_t + 4;
+            // X's atom, then W's (the second 128-row block of W 4 columns on,
+            // as the block-scaled MMA reads a 256-row B)
+            const uint32_t sf_t = tmem + sf_col0 + static_cast<uint32_t>(s * C::SF_COLS);
+            const uint32_t sfa_t = C::WIDE ? sf_t + 8 : sf_t;
+            const uint32_t sfb_t = C::WIDE ? sf_t : sf_t + 4;
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k)
               mma_mxf8f6f4(d, adesc + 2 * k, bdesc + 2 * k,
@@ -2329,17 +2356,23 @@ fp8_status_t launch_gemm_mx(const uint8_t *a, const uint8_t *sfa, const uint8_t 
   if (mode == 2)
     return launch_gemm_mx_pairs(a, sfa, b, sfb, a_fmt, b_fmt, out, M, N, K, dev_status, stream, wait_ns);
   constexpr int BN = MX_BN, ST = MX_STAGES, NACC = MX_NACC;
-  using C = AccCfg<KIND_MX8, BN, ST, NACC>;
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, a, M, K, K, BM, BK) || !make_tmap_u8(&tb, b, N, K, K, BN, BK)) return FP8_ERR_CUDA;
-  auto kern = gemm_tmem_kernel<KIND_MX8, BN, ST, NACC>;
-  if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
   const int ntiles = static_cast<int>(((M + 127) / 128) * ((N + BN - 1) / BN));
-  kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
-      ta, tb, nullptr, 0, nullptr, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-      idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status, raster_group(M, K), wait_ns);
-  note_launches(1);
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  auto run = [&](auto kind) -> fp8_status_t {
+    constexpr int KIND = decltype(kind)::value;
+    using C = AccCfg<KIND, BN, ST, NACC>;
+    auto kern = gemm_tmem_kernel<KIND, BN, ST, NACC>;
+    if (!ensure_smem(kern, C::SMEM)) return FP8_ERR_CUDA;
+    kern<<<persistent_grid(ntiles), C::THREADS, C::SMEM, stream>>>(
+        ta, tb, nullptr, 0, nullptr, 0, sfa, sfb, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+        idesc_mxf8f6f4(a_fmt, b_fmt, BM, BN, 0, 0), dev_status, raster_group(M, K), wait_ns);
+    note_launches(1);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  };
+  // mode 3: the scales in the staged-four-times layout
+  if (mode == 3) return run(std::integral_constant<int, KIND_MX8W>{});
+  return run(std::integral_constant<int, KIND_MX8>{});
 }
 
 // NVFP4: a and b are packed E2M1 [M x K/2], [N x K/2] bytes (K % 256 == 0);

@@ -208,6 +208,15 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, ui
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
+// 128 rows of 32 / 16 bytes (shared memory, described by sdesc) -> tensor-
+// memory lanes 0-127, eight / four 32-bit columns from taddr: row r's bytes
+// land in lane r, in order.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -352,16 +361,19 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
-// Descriptor of an unswizzled 32 x 16-byte block (eight-row core matrices of
-// 128 contiguous bytes, 128 bytes apart).
-__device__ __forceinline__ uint64_t sdesc_plain_32x16(uint32_t saddr) {
+// Descriptor of unswizzled shared memory: eight-row core matrices of 128
+// contiguous bytes (8 rows x 16 bytes), the same rows' next 16-byte column
+// chunk lbo bytes on, the next 8 rows sbo bytes on.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(128u >> 4) << 16;
-  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(lbo >> 4) << 16;  // leading byte offset: the next 16-byte column chunk
+  d |= static_cast<uint64_t>(sbo >> 4) << 32;  // stride byte offset: the next group of 8 rows
   d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
+// a 32 x 16-byte block (its four core matrices contiguous)
+__device__ __forceinline__ uint64_t sdesc_plain_32x16(uint32_t saddr) { return sdesc_plain(saddr, 128, 128); }
 
 // Instruction descriptor for kind::f8f6f4: fp32 accumulator, A/B formats
 // (0 = E4M3, 1 = E5M2), both operands K-major, tile M x N.

@@ -59,6 +59,12 @@ __device__ __forceinline__ int64_t mx_tiled_index(int64_t r, int64_t j, int64_t 
   const int64_t col_blocks = (ngroups + 3) >> 2;
   return (((r >> 7) * col_blocks + (j >> 2)) << 9) + ((r & 31) << 4) + (((r & 127) >> 5) << 2) + (j & 3);
 }
+// The same byte in the staged-four-times layout (each 512-byte block stored
+// four times in a row): its first copy; the others follow 512 bytes apart.
+__device__ __forceinline__ int64_t mx_tiled_x4_index(int64_t r, int64_t j, int64_t ngroups) {
+  const int64_t t = mx_tiled_index(r, j, ngroups);
+  return ((t >> 9) << 11) + (t & 511);
+}
 
 // ------------------------------------------------------------ group kernels
 // GROUP elements share a scale (128: 1x128 tile, 32: MX). A warp task is one
@@ -79,7 +85,9 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&m)[N], int i) {
   }
 }
 
-template <int FMT, int GROUP, bool MX, bool TILED, int VPL = kVecPerLane>
+// TILED (MX): 0 linear scales, 1 the tensor-core tiled layout, 4 that layout
+// with each 512-byte block stored four times in a row
+template <int FMT, int GROUP, bool MX, int TILED, int VPL = kVecPerLane>
 __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
                                                                int64_t ldq, void *__restrict__ scales) {
@@ -146,9 +154,17 @@ __global__ void __launch_bounds__(kThreads) quant_group_kernel(const uint16_t *_
           const int64_t j = pcv / TPG;
           const int64_t ng = cols / 32;
           uint8_t *sf = static_cast<uint8_t *>(scales);
-          const int64_t si = TILED ? mx_tiled_index(r, j, ng) : r * ng + j;
-          if (FP8BS_GUARD(si, 1, TILED ? ((rows + 127) / 128) * ((ng + 3) / 4) * 512 : rows * ng))
-            sf[si] = static_cast<uint8_t>(e + 127);
+          if constexpr (TILED == 4) {
+            const int64_t si = mx_tiled_x4_index(r, j, ng);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (FP8BS_GUARD(si + 512 * k, 1, ((rows + 127) / 128) * ((ng + 3) / 4) * 2048))
+                sf[si + 512 * k] = static_cast<uint8_t>(e + 127);
+          } else {
+            const int64_t si = TILED ? mx_tiled_index(r, j, ng) : r * ng + j;
+            if (FP8BS_GUARD(si, 1, TILED ? ((rows + 127) / 128) * ((ng + 3) / 4) * 512 : rows * ng))
+              sf[si] = static_cast<uint8_t>(e + 127);
+          }
         }
       } else {
         float s;
@@ -654,7 +670,9 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t *__rest
         case FP8_GRAN_CHANNEL: s = 1.0f; break;
         default: {
           const int64_t ng = cols >> 5;
-          const uint8_t e = sb[sf_layout == FP8_SF_TCGEN05 ? mx_tiled_index(r, c >> 5, ng) : r * ng + (c >> 5)];
+          const uint8_t e = sb[sf_layout == FP8_SF_TCGEN05      ? mx_tiled_index(r, c >> 5, ng)
+                               : sf_layout == FP8_SF_TCGEN05_X4 ? mx_tiled_x4_index(r, c >> 5, ng)
+                                                                : r * ng + (c >> 5)];
           s = e == 0xff ? __uint_as_float(0x7fc00000u) : exp2_exact(static_cast<int>(e) - 127);
         }
       }
@@ -795,8 +813,8 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
     case FP8_GRAN_TILE_1x128: {
       const int64_t tile_tasks = rows * ((cols / 8 + 32 * kTileVecPerLane - 1) / (32 * kTileVecPerLane));
 #define FP8BS_TILE(F)                                                                                   \
-  quant_group_kernel<F, 128, false, false, kTileVecPerLane>                                                 \
-      <<<stream_grid(quant_group_kernel<F, 128, false, false, kTileVecPerLane>, tile_tasks), kThreads, 0, \
+  quant_group_kernel<F, 128, false, 0, kTileVecPerLane>                                                 \
+      <<<stream_grid(quant_group_kernel<F, 128, false, 0, kTileVecPerLane>, tile_tasks), kThreads, 0, \
          stream>>>(x, rows, cols, ld_x, q, ld_q, scales)
       if (e4)
         FP8BS_TILE(FP8_E4M3);
@@ -818,24 +836,30 @@ fp8_status_t launch_quantize(const uint16_t *x, int64_t rows, int64_t cols, int6
       break;
     }
     case FP8_GRAN_MX32: {
-      const bool tiled = sf_layout == FP8_SF_TCGEN05;
+      // 0 linear, 1 tiled, 4 tiled and staged four times
+      const int tiled = sf_layout == FP8_SF_TCGEN05 ? 1 : (sf_layout == FP8_SF_TCGEN05_X4 ? 4 : 0);
       const int64_t mx_tasks = rows * ((cols / 8 + 32 * kMxVecPerLane - 1) / (32 * kMxVecPerLane));
       if (tiled && (rows % 128 != 0 || cols % 128 != 0)) {
-        const size_t bytes = static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) * 512;
+        const size_t bytes =
+            static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((cols + 127) / 128) * 512 * tiled;
         if (cudaMemsetAsync(scales, 0, bytes, stream) != cudaSuccess) return FP8_ERR_CUDA;
       }
 #define FP8BS_MX(F, T)                                                                              \
   quant_group_kernel<F, 32, true, T, kMxVecPerLane>                                                    \
       <<<stream_grid(quant_group_kernel<F, 32, true, T, kMxVecPerLane>, mx_tasks), kThreads, 0, stream>>>( \
           x, rows, cols, ld_x, q, ld_q, scales)
-      if (e4 && tiled)
-        FP8BS_MX(FP8_E4M3, true);
+      if (e4 && tiled == 4)
+        FP8BS_MX(FP8_E4M3, 4);
+      else if (e4 && tiled)
+        FP8BS_MX(FP8_E4M3, 1);
       else if (e4)
-        FP8BS_MX(FP8_E4M3, false);
+        FP8BS_MX(FP8_E4M3, 0);
+      else if (tiled == 4)
+        FP8BS_MX(FP8_E5M2, 4);
       else if (tiled)
-        FP8BS_MX(FP8_E5M2, true);
+        FP8BS_MX(FP8_E5M2, 1);
       else
-        FP8BS_MX(FP8_E5M2, false);
+        FP8BS_MX(FP8_E5M2, 0);
 #undef FP8BS_MX
       ++launches;
       break;

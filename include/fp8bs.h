@@ -84,8 +84,14 @@ typedef enum {
  *            bytes, blocks row-block-major; inside a block the byte of
  *            (row r, group j) is at (r%32)*16 + ((r%128)/32)*4 + (j%4).
  *            Size: ceil(rows/128) * ceil(cols/128) * 512 bytes; padding bytes
- *            are written as 0. */
-typedef enum { FP8_SF_LINEAR = 0, FP8_SF_TCGEN05 = 1 } fp8_sf_layout_t;
+ *            are written as 0.
+ *   TCGEN05_X4  (MX-32 only) the TCGEN05 layout with each 512-byte block
+ *            stored four times in a row (2048 bytes per block; block b's
+ *            copies at 2048*b + 512*i, i = 0..3). A layout of this library,
+ *            not of the pages: the GEMM moves such blocks into tensor memory
+ *            with fewer, wider copies (fp8_gemm_mx_x4). Size: 4 times
+ *            TCGEN05's. */
+typedef enum { FP8_SF_LINEAR = 0, FP8_SF_TCGEN05 = 1, FP8_SF_TCGEN05_X4 = 2 } fp8_sf_layout_t;
 
 typedef enum {
   FP8_OK = 0,
@@ -232,6 +238,14 @@ fp8_status_t fp8_gemm_blockscaled_quantized_out(const void *a_dev, const float *
 fp8_status_t fp8_gemm_mx(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
                          fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
                          int *dev_status, fp8_stream_t stream);
+
+/* fp8_gemm_mx with a_sf_dev / b_sf_dev in the FP8_SF_TCGEN05_X4 layout (as
+ * fp8_quantize writes it for FP8_GRAN_MX32): the same product, bit for bit;
+ * each stage's scale blocks reach tensor memory in two copies instead of
+ * three. Same rules as fp8_gemm_mx. */
+fp8_status_t fp8_gemm_mx_x4(const void *a_dev, const uint8_t *a_sf_dev, const void *b_dev, const uint8_t *b_sf_dev,
+                            fp8_format_t a_fmt, fp8_format_t b_fmt, void *out_dev, int64_t M, int64_t N, int64_t K,
+                            int *dev_status, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------ NVFP4
  * "Low precision: FP8, FP4, and microscaling" (NVFP4 paragraph): blocks of 16

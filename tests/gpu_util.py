@@ -101,3 +101,11 @@ class Guarded:
         lo = self.raw[:GUARD_BYTES]
         hi = self.raw[GUARD_BYTES + self.nbytes:]
         return bool((lo == GUARD_BYTE).all()) and bool((hi == GUARD_BYTE).all())
+
+
+def x4_layout(sf_tiled):
+    """Scales in the tensor-core tiled layout -> the staged-four-times layout
+    (each 512-byte block stored four times in a row). Layout plumbing only: the
+    bytes are the oracle's, repeated."""
+    blocks = np.asarray(sf_tiled, dtype=np.uint8).reshape(-1, 1, 512)
+    return np.ascontiguousarray(np.repeat(blocks, 4, axis=1)).reshape(-1)

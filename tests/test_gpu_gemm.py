@@ -11,7 +11,7 @@ import torch
 import oracle
 from fp8_block_scaled_04_gb300 import binding as fb
 from fp8_block_scaled_04_gb300 import synth
-from gpu_util import bf16_host, out_f64, to_dev_bf16, within_tolerance
+from gpu_util import bf16_host, out_f64, to_dev_bf16, within_tolerance, x4_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -217,6 +217,27 @@ def test_mx_shapes(M, N, K):
     out = _run_mx(qa, sfa, qb, sfb)
     ref, bound = oracle.gemm(qa, sfa, fb.MX32, qb, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05)
     tol = within_tolerance(out_f64(out), ref, bound)
+    assert tol.bad == 0, tol
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 256, 512), (130, 272, 416), (1, 16, 32), (300, 640, 1024),
+                                   (1024, 1536, 4096), (2304, 512, 640)])
+def test_mx_x4_layout_same_output_as_tiled(M, N, K):
+    """fp8_gemm_mx_x4 on the staged-four-times scales: the same tensor-memory
+    scale contents as fp8_gemm_mx, so the same output bit for bit, and within
+    the tolerance of the oracle."""
+    x = synth.bf16_matrix(M, K, 1.0, 60 + M, 61, 0.005, 50.0)
+    w = synth.bf16_matrix(N, K, 1.0, 62 + N, 63, 0.005, 50.0)
+    qa, sfa, qb, sfb = _quant_pair(x, w, fb.MX32, fb.MX32, layout=fb.SF_TCGEN05)
+    out = _run_mx(qa, sfa, qb, sfb)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out4 = fb.gemm_mx(torch.from_numpy(qa).cuda(), torch.from_numpy(x4_layout(sfa)).cuda(), torch.from_numpy(qb).cuda(),
+                      torch.from_numpy(x4_layout(sfb)).cuda(), status=status, sf_layout=fb.SF_TCGEN05_X4)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out.view(torch.int16), out4.view(torch.int16))
+    ref, bound = oracle.gemm(qa, sfa, fb.MX32, qb, sfb, fb.MX32, a_sf=fb.SF_TCGEN05, b_sf=fb.SF_TCGEN05)
+    tol = within_tolerance(out_f64(out4), ref, bound)
     assert tol.bad == 0, tol
 
 

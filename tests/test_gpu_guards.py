@@ -13,7 +13,7 @@ import torch
 import oracle
 from fp8_block_scaled_04_gb300 import binding as fb
 from fp8_block_scaled_04_gb300 import synth
-from gpu_util import Guarded, f32_bits, out_f64, to_dev_bf16, within_tolerance
+from gpu_util import Guarded, f32_bits, out_f64, to_dev_bf16, within_tolerance, x4_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -101,6 +101,18 @@ def test_mx_and_nvfp4_stay_in_bounds(M, N, K):
         assert out.intact(), kernel
         tol = within_tolerance(out_f64(out.t), ref, bound)
         assert tol.bad == 0, (kernel, tol)
+    # the staged-four-times scale layout: quantizer scales and the GEMM's output
+    sx4 = Guarded((fb.scales_bytes(M, K, fb.MX32, fb.SF_TCGEN05_X4),), torch.uint8)
+    qx4 = Guarded((M, K), torch.uint8)
+    fb.quantize(to_dev_bf16(x), fb.E4M3, fb.MX32, fb.SF_TCGEN05_X4, q=qx4.t, scales=sx4.t)
+    assert sx4.intact() and qx4.intact()
+    assert np.array_equal(sx4.t.cpu().numpy(), x4_layout(sfa))
+    sw4 = torch.from_numpy(x4_layout(sfb)).cuda()
+    out4 = Guarded((M, N), torch.bfloat16)
+    fb.gemm_mx(qx4.t, sx4.t, torch.from_numpy(qb).cuda(), sw4, out=out4.t, sf_layout=fb.SF_TCGEN05_X4)
+    assert out4.intact()
+    tol = within_tolerance(out_f64(out4.t), ref, bound)
+    assert tol.bad == 0, ("x4", tol)
     # NVFP4: codes, padded tiled scale atoms, tensor scale, dequantized output, GEMM output
     xd = to_dev_bf16(x)
     q4 = Guarded((M, K // 2), torch.uint8)

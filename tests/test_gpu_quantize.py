@@ -9,7 +9,7 @@ import torch
 import oracle
 from fp8_block_scaled_04_gb300 import binding as fb
 from fp8_block_scaled_04_gb300 import synth
-from gpu_util import bf16_host, f32_bits, to_dev_bf16
+from gpu_util import bf16_host, f32_bits, to_dev_bf16, x4_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +49,26 @@ def test_quantize_mx_tiled_layout_bit_exact(fmt, shape):
     rows, cols = shape
     x = synth.bf16_matrix(rows, cols, 1.0, 77, 78, 0.02, 30.0)
     _check_quant(x, fmt, fb.MX32, fb.SF_TCGEN05)
+
+
+@pytest.mark.parametrize("shape", [(130, 640), (128, 512), (257, 160), (1, 32)])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quantize_mx_x4_layout_bit_exact(fmt, shape):
+    """MX-32 scales in the staged-four-times layout: codes equal the oracle's and
+    the scale bytes equal the oracle's tiled bytes with each 512-byte block
+    repeated four times (padding of partial blocks zero in every copy); the
+    dequantizer reads them back to the oracle's values."""
+    rows, cols = shape
+    x = synth.bf16_matrix(rows, cols, 1.0, 79, 80, 0.02, 30.0)
+    q, s = fb.quantize(to_dev_bf16(x), fmt, fb.MX32, fb.SF_TCGEN05_X4)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quantize(x, fmt, fb.MX32, fb.SF_TCGEN05)
+    assert s.numel() == fb.scales_bytes(rows, cols, fb.MX32, fb.SF_TCGEN05_X4) == 4 * os_.size
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), x4_layout(os_))
+    out = fb.dequantize(q, s, fmt, fb.MX32, fb.SF_TCGEN05_X4)
+    ref = oracle.dequantize(oq, os_, fmt, fb.MX32, fb.SF_TCGEN05)
+    assert np.array_equal(bf16_host(out), ref)
 
 
 @pytest.mark.parametrize("gran", [fb.TENSOR, fb.TOKEN, fb.TILE_1x128, fb.MX32])
