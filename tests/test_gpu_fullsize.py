@@ -9,7 +9,7 @@ import torch
 import oracle
 from fp8_block_scaled_04_gb300 import binding as fb
 from fp8_block_scaled_04_gb300 import synth
-from gpu_util import f32_bits, out_f64, to_dev_bf16, within_tolerance
+from gpu_util import f32_bits, out_f64, to_dev_bf16, within_tolerance, x4_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -104,3 +104,14 @@ def test_mx_gemm_full_size_sampled_rows():
     got = out_f64(out[torch.from_numpy(rows).cuda()])
     tol = within_tolerance(got, ref, bound)
     assert tol.bad == 0, tol
+    # the path the bench times first: scales quantized straight into the
+    # staged-four-times layout, fp8_gemm_mx_x4 (the same output, bit for bit)
+    _, sfa4_d = fb.quantize(to_dev_bf16(x), fb.E4M3, fb.MX32, fb.SF_TCGEN05_X4)
+    _, sfb4_d = fb.quantize(to_dev_bf16(w), fb.E4M3, fb.MX32, fb.SF_TCGEN05_X4)
+    assert np.array_equal(sfa4_d.cpu().numpy(), x4_layout(sfa)) and np.array_equal(sfb4_d.cpu().numpy(), x4_layout(sfb))
+    out4 = fb.gemm_mx(qa_d, sfa4_d, qb_d, sfb4_d, status=status, sf_layout=fb.SF_TCGEN05_X4)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out.view(torch.int16), out4.view(torch.int16))
+    tol4 = within_tolerance(out_f64(out4[torch.from_numpy(rows).cuda()]), ref, bound)
+    assert tol4.bad == 0, tol4
