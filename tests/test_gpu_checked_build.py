@@ -46,7 +46,8 @@ def _eq(a, b):
 
 
 GRANS = [(fb.TENSOR, fb.SF_LINEAR), (fb.TOKEN, fb.SF_LINEAR), (fb.TILE_1x128, fb.SF_LINEAR),
-         (fb.BLOCK_128x128, fb.SF_LINEAR), (fb.MX32, fb.SF_LINEAR), (fb.MX32, fb.SF_TCGEN05), (fb.CHANNEL, fb.SF_LINEAR)]
+         (fb.BLOCK_128x128, fb.SF_LINEAR), (fb.MX32, fb.SF_LINEAR), (fb.MX32, fb.SF_TCGEN05),
+         (fb.MX32, fb.SF_TCGEN05_X4), (fb.CHANNEL, fb.SF_LINEAR)]
 
 
 @pytest.mark.parametrize("shape", [(1, 128), (7, 384), (130, 640), (257, 1152), (3, 17408)])
@@ -93,6 +94,9 @@ def test_gemms_record_no_stray_store(checked, M, N, K):
     ma, msa = fb.quantize(x, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     mb, msb = fb.quantize(w, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
     _eq(*_both(checked, lambda: fb.gemm_mx(ma, msa, mb, msb)))
+    _, msa4 = fb.quantize(x, fb.E4M3, fb.MX32, fb.SF_TCGEN05_X4)
+    _, msb4 = fb.quantize(w, fb.E4M3, fb.MX32, fb.SF_TCGEN05_X4)
+    _eq(*_both(checked, lambda: fb.gemm_mx(ma, msa4, mb, msb4, sf_layout=fb.SF_TCGEN05_X4)))
     _eq(*_both(checked, lambda: fb.debug_gemm_mx_kernel("pairs", ma, msa, mb, msb)))
     if K % 256 == 0:
         na, nsa, nta = fb.quantize_nvfp4(x)
