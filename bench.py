@@ -776,6 +776,31 @@ def cpu_baselines_other(extra, synth, rows_sweep: int = 512, rows_mx: int = 16):
         extra["mx_gemm_8192"]["cpu_baseline"] = {"value": round(2.0 * rows_mx * S * S / dt / 1e12, 5),
                                                  "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                                  "sample": "first %d of 8192 rows of X, all of W, fp64 sums" % rows_mx}
+    nq = extra.get("nvfp4_quantize_16384x8192")
+    if nq is not None:
+        # the NVFP4 quantizer: both modes on the sample rows (two passes: the
+        # sample's own tensor amax, then the encode)
+        xs4 = synth.sweep_x(rows_sweep, C)
+        for mode, static in (("two_pass", None), ("static_scale", 0.01)):
+            if mode not in nq:
+                continue
+            t0 = time.perf_counter()
+            oracle.quantize_nvfp4(xs4, oracle.SF_TILED, static)
+            dt = time.perf_counter() - t0
+            byts = nq[mode]["algorithmic_bytes"] * rows_sweep / 16384.0
+            nq[mode]["cpu_baseline"] = {"value": round(byts / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+                                        "kind": "oracle", "sample": "first %d of 16384 rows" % rows_sweep}
+    if "nvfp4_gemm_8192" in extra:
+        S = 8192
+        aq, asf, ats = oracle.quantize_nvfp4(synth.mx_x(rows_mx, S), oracle.SF_TILED)
+        bq, bsf, bts = oracle.quantize_nvfp4(synth.mx_w(S, S), oracle.SF_TILED)
+        t0 = time.perf_counter()
+        oracle.gemm_nvfp4(aq, asf, ats, bq, bsf, bts, oracle.SF_TILED)
+        dt = time.perf_counter() - t0
+        extra["nvfp4_gemm_8192"]["cpu_baseline"] = {"value": round(2.0 * rows_mx * S * S / dt / 1e12, 5),
+                                                    "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                                    "sample": "first %d of 8192 rows of X (tensor scale from those "
+                                                              "rows), all of W, fp64 sums" % rows_mx}
 
 
 def cpu_baseline_sample(x_host, w_host, target_s: float = 10.0):
