@@ -25,6 +25,8 @@
 // gemm_tmem_kernel<KIND_MX8> -- MXFP8: kind::mxf8f6f4.block_scale applies one
 //   UE8M0 scale per 32 K-elements inside the tensor core ("Low precision",
 //   microscaling); scale-factor atoms go smem -> tensor memory with tcgen05.cp.
+//   KIND_MX8W is the same product on scales staged four times over, which
+//   tensor memory takes in two wide copies per stage instead of three.
 // gemm_tmem_kernel<KIND_NVF4> -- NVFP4: kind::mxf4nvf4.block_scale.scale_vec::4X
 //   with E2M1 operands and one E4M3 scale per 16 K-elements; the two fp32
 //   tensor scales multiply the accumulator in the epilogue.
