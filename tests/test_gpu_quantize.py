@@ -71,6 +71,27 @@ def test_quantize_mx_x4_layout_bit_exact(fmt, shape):
     assert np.array_equal(bf16_host(out), ref)
 
 
+@pytest.mark.parametrize("layout", [fb.SF_TCGEN05, fb.SF_TCGEN05_X4])
+@pytest.mark.parametrize("shape", [(130, 640), (257, 160)])
+def test_quantize_mx_tiled_scales_only_4_byte_aligned(layout, shape):
+    """A tiled scale array that is 4- but not 16-byte aligned takes the
+    byte-store kernel instead of the block kernel: the same bytes."""
+    rows, cols = shape
+    x = synth.bf16_matrix(rows, cols, 1.0, 81, 82, 0.02, 30.0)
+    n = fb.scales_bytes(rows, cols, fb.MX32, layout)
+    big = torch.full((n + 16,), 0x5A, dtype=torch.uint8, device="cuda")
+    s = big[4:4 + n]
+    assert s.data_ptr() % 16 == 4
+    q, _ = fb.quantize(to_dev_bf16(x), fb.E4M3, fb.MX32, layout, scales=s)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quantize(x, fb.E4M3, fb.MX32, fb.SF_TCGEN05)
+    want = os_ if layout == fb.SF_TCGEN05 else x4_layout(os_)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    got = big.cpu().numpy()
+    assert np.array_equal(got[4:4 + n], want)
+    assert (got[:4] == 0x5A).all() and (got[4 + n:] == 0x5A).all()
+
+
 @pytest.mark.parametrize("gran", [fb.TENSOR, fb.TOKEN, fb.TILE_1x128, fb.MX32])
 def test_extreme_values(gran):
     rng = np.random.default_rng(5)
